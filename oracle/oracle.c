@@ -1,0 +1,239 @@
+/*
+ * Oracle for the small-M quantized weight GEMMs: plain, slow, obviously correct
+ * CPU code.  TEST INFRASTRUCTURE ONLY: the tests, the package smoke check and the
+ * benchmark's CPU-baseline leg use it; the library's compute path never does.
+ * It shares no code, header, table or helper with the CUDA library.
+ *
+ * Sources (web pages; section names as printed there):
+ *  [W8A8] "INT8 W8A8 GEMM - Decode (M <= 32) - gfx928 / SGLang TP4", operator line:
+ *         x_q[M,K] int8 @ W[K,N] int8 -> int32 -> * x_scale[M,1] * weight_scale[N,1].T -> bf16[M,N].
+ *         Section 1.1, "Cross-shape rules that held": int32 accumulation that is k-ascending per
+ *         split, then an ascending sum over splits; "[0,K) exactly once".
+ *  [Q8_0] "sycl: STRATA_HC_Q8=1 reads the Q8_0 hyper-connection projections", section
+ *         "What changed": Q8_0 weights as blocks of 32 int8 quants with one fp16 scale,
+ *         dequantised as w = d * q; the split layout (every row's quants row-major, then every
+ *         row's fp16 scales); the parity test's FP64 reference computed from the very Q8_0
+ *         bytes the kernel reads.
+ *
+ * Readings where the pages leave a step open (also listed in the design notes):
+ *  - The W8A8 epilogue is (float(acc) * x_scale[m]) * w_scale[n], each step an IEEE fp32
+ *    multiply rounded to nearest even, then rounded to nearest even into bfloat16.  The pages
+ *    only say "scales ... bf16"; the order is the one the benchmark spec fixes.
+ *  - Q8_0 blocks run along K inside each weight row n; d has shape [N, K/32].
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -shared -fPIC (see build.py).
+ * Every float operation below is a single IEEE operation: no contraction, no x87.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <math.h>
+
+/* ---------------------------------------------------------------------------------------
+ * bfloat16 / float16 scalars, written from the IEEE-754 definitions.
+ * ------------------------------------------------------------------------------------- */
+
+/* float32 -> bfloat16 bits, round to nearest, ties to even.  bfloat16 keeps the top 16 bits
+ * of the float32 encoding; the discarded low half decides the rounding: above 0x8000 rounds
+ * up, below rounds down, exactly 0x8000 rounds to the even upper half.  NaN inputs keep a
+ * quiet NaN (never reached by the W8A8 epilogue, whose values are finite). */
+uint16_t oracle_bf16_from_f32(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t upper = u >> 16;
+    uint32_t lower = u & 0xFFFFu;
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))
+        upper += 1u;               /* a carry into the exponent is the correct rounding */
+    return (uint16_t)upper;
+}
+
+double oracle_bf16_to_f64(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+/* IEEE binary16 -> double: sign, 5-bit exponent (bias 15), 10-bit fraction. */
+double oracle_f16_to_f64(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1F;
+    int frac = h & 0x3FF;
+    double v;
+    if (e == 0)
+        v = ldexp((double)frac, -24);                  /* subnormal: frac * 2^-14 * 2^-10 */
+    else if (e == 31)
+        v = frac ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + frac), e - 25);      /* (1 + frac/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* ---------------------------------------------------------------------------------------
+ * W8A8 decode GEMM  [W8A8] operator line.
+ * ------------------------------------------------------------------------------------- */
+
+/* acc[m][n] = sum_{k=0}^{K-1} x_q[m][k] * W[k][n], summed in int64 and then checked to fit
+ * int32 (the operator's accumulator type).  x_q is [M,K] row-major, W is [K,N] row-major.
+ * Returns 0, or -1 if some sum leaves the int32 range. */
+int oracle_w8a8_acc(const int8_t* x_q, const int8_t* W, int M, int K, int N, int32_t* acc) {
+    int64_t* row = (int64_t*)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
+    int rc = 0;
+    if (!row) return -2;
+    for (int m = 0; m < M; ++m) {
+        for (int n = 0; n < N; ++n) row[n] = 0;
+        for (int k = 0; k < K; ++k) {
+            int64_t xv = x_q[(size_t)m * K + k];
+            const int8_t* wk = W + (size_t)k * N;
+            for (int n = 0; n < N; ++n) row[n] += xv * (int64_t)wk[n];
+        }
+        for (int n = 0; n < N; ++n) {
+            if (row[n] > INT32_MAX || row[n] < INT32_MIN) rc = -1;
+            acc[(size_t)m * N + n] = (int32_t)row[n];
+        }
+    }
+    free(row);
+    return rc;
+}
+
+/* The same sums taken the way a split-K kernel takes them ([W8A8] section 1.1): the K range is
+ * cut at bounds[0]=0 < bounds[1] < ... < bounds[parts]=K; each slice is summed k-ascending in
+ * int32, and the slice sums are added in ascending slice order in int32.  Returns -1 if the
+ * bounds do not cover [0,K) exactly once in ascending order. */
+int oracle_w8a8_acc_split(const int8_t* x_q, const int8_t* W, int M, int K, int N,
+                          const int* bounds, int parts, int32_t* acc) {
+    if (parts < 1 || bounds[0] != 0 || bounds[parts] != K) return -1;
+    for (int p = 0; p < parts; ++p)
+        if (bounds[p + 1] < bounds[p]) return -1;
+    for (int m = 0; m < M; ++m) {
+        for (int n = 0; n < N; ++n) {
+            int32_t total = 0;
+            for (int p = 0; p < parts; ++p) {
+                int32_t slice = 0;
+                for (int k = bounds[p]; k < bounds[p + 1]; ++k)
+                    slice += (int32_t)x_q[(size_t)m * K + k] * (int32_t)W[(size_t)k * N + n];
+                total += slice;
+            }
+            acc[(size_t)m * N + n] = total;
+        }
+    }
+    return 0;
+}
+
+/* out[m][n] = bf16_rne( fp32( fp32(float(acc[m][n]) * x_scale[m]) * w_scale[n] ) ).
+ * (float)acc is the C conversion, which rounds to nearest even for |acc| > 2^24. */
+void oracle_w8a8_epilogue(const int32_t* acc, const float* x_scale, const float* w_scale,
+                          int M, int N, uint16_t* out) {
+    for (int m = 0; m < M; ++m) {
+        for (int n = 0; n < N; ++n) {
+            float f = (float)acc[(size_t)m * N + n];
+            volatile float a = f * x_scale[m];       /* volatile: keep two separate roundings */
+            volatile float b = a * w_scale[n];
+            out[(size_t)m * N + n] = oracle_bf16_from_f32(b);
+        }
+    }
+}
+
+/* Whole operator: accumulate, then the scale / bf16 epilogue.  acc may be NULL. */
+int oracle_w8a8_gemm(const int8_t* x_q, const float* x_scale, const int8_t* W, const float* w_scale,
+                     int M, int K, int N, uint16_t* out, int32_t* acc) {
+    int32_t* a = acc ? acc : (int32_t*)malloc(sizeof(int32_t) * (size_t)M * (size_t)N + 4);
+    if (!a) return -2;
+    int rc = oracle_w8a8_acc(x_q, W, M, K, N, a);
+    oracle_w8a8_epilogue(a, x_scale, w_scale, M, N, out);
+    if (!acc) free(a);
+    return rc;
+}
+
+/* ---------------------------------------------------------------------------------------
+ * Q8_0 weight GEMV  [Q8_0] section "What changed".
+ * ------------------------------------------------------------------------------------- */
+
+/* y[t][n] = sum_k x[t][k] * (d[n][k/32] * q[n][k]) in double, from the very bf16 / fp16 /
+ * int8 bytes the kernel reads.  x: bf16 bits [T,K]; q: int8 [N,K]; d: fp16 bits [N,K/32]. */
+void oracle_q8_0_gemv(const uint16_t* x, const int8_t* q, const uint16_t* d,
+                      int T, int K, int N, double* y) {
+    int nb = K / 32;
+    for (int t = 0; t < T; ++t) {
+        for (int n = 0; n < N; ++n) {
+            double s = 0.0;
+            for (int k = 0; k < K; ++k) {
+                double w = oracle_f16_to_f64(d[(size_t)n * nb + k / 32]) * (double)q[(size_t)n * K + k];
+                s += oracle_bf16_to_f64(x[(size_t)t * K + k]) * w;
+            }
+            y[(size_t)t * N + n] = s;
+        }
+    }
+}
+
+/* Euclidean norms used by the per-output error bound: xnorm[t] = ||x_t||_2 and
+ * wnorm[n] = ||w_n||_2 with w_n the dequantised weight row (w = d * q). */
+void oracle_q8_0_norms(const uint16_t* x, const int8_t* q, const uint16_t* d,
+                       int T, int K, int N, double* xnorm, double* wnorm) {
+    int nb = K / 32;
+    for (int t = 0; t < T; ++t) {
+        double s = 0.0;
+        for (int k = 0; k < K; ++k) {
+            double v = oracle_bf16_to_f64(x[(size_t)t * K + k]);
+            s += v * v;
+        }
+        xnorm[t] = sqrt(s);
+    }
+    for (int n = 0; n < N; ++n) {
+        double s = 0.0;
+        for (int k = 0; k < K; ++k) {
+            double w = oracle_f16_to_f64(d[(size_t)n * nb + k / 32]) * (double)q[(size_t)n * K + k];
+            s += w * w;
+        }
+        wnorm[n] = sqrt(s);
+    }
+}
+
+/* ggml-style interleaved Q8_0 rows (per block: fp16 scale, then 32 int8 quants; 34 bytes)
+ * -> the split layout (all quants [N][K], then all scales [N][K/32]).  [Q8_0] "What changed":
+ * "the same bytes as ggml's 34-byte blocks, reordered". */
+void oracle_q8_0_split_from_blocks(const uint8_t* blocks, int K, int N, int8_t* q, uint16_t* d) {
+    int nb = K / 32;
+    for (int n = 0; n < N; ++n) {
+        for (int b = 0; b < nb; ++b) {
+            const uint8_t* blk = blocks + ((size_t)n * nb + b) * 34;
+            d[(size_t)n * nb + b] = (uint16_t)(blk[0] | (blk[1] << 8));
+            for (int j = 0; j < 32; ++j) q[(size_t)n * K + (size_t)b * 32 + j] = (int8_t)blk[2 + j];
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------------------------
+ * Packed weight layout of w8a8_pack_weights, written out from its documented definition
+ * (the library header states it; [W8A8] section 1.1 asks for the cold weight to be packed
+ * once, outside the timed region, into the fragment's layout).
+ *
+ *   N is padded to Np = 64 * ceil(N / 64); KB = K / 32.
+ *   byte (t, kb, s, lane, j), t < Np/64, kb < KB, s < 4, lane < 32, j < 16, sits at
+ *     ((((t * KB + kb) * 4 + s) * 32 + lane) * 16 + j)
+ *   and holds W[k][n] XOR 0x80 (offset binary), or 0x80 for a padding row n >= N, with
+ *     g = lane / 4, c = lane % 4, w = j / 4, b = j % 4,
+ *     n = 64 t + 16 s + g + 8 (w % 2),   k = 32 kb + 8 c + 4 (w / 2) + b.
+ * ------------------------------------------------------------------------------------- */
+size_t oracle_w8a8_packed_bytes(int K, int N) {
+    size_t np = (size_t)((N + 63) / 64) * 64;
+    return np * (size_t)K;
+}
+
+void oracle_w8a8_pack(const int8_t* W, int K, int N, uint8_t* packed) {
+    int KB = K / 32;
+    int tiles = (N + 63) / 64;
+    for (int t = 0; t < tiles; ++t)
+        for (int kb = 0; kb < KB; ++kb)
+            for (int s = 0; s < 4; ++s)
+                for (int lane = 0; lane < 32; ++lane)
+                    for (int j = 0; j < 16; ++j) {
+                        int g = lane / 4, c = lane % 4, w = j / 4, b = j % 4;
+                        int n = 64 * t + 16 * s + g + 8 * (w % 2);
+                        int k = 32 * kb + 8 * c + 4 * (w / 2) + b;
+                        size_t off = ((((size_t)t * KB + kb) * 4 + s) * 32 + lane) * 16 + j;
+                        packed[off] = n < N ? (uint8_t)(((uint8_t)W[(size_t)k * N + n]) ^ 0x80u) : 0x80u;
+                    }
+}
