@@ -1,0 +1,496 @@
+#!/usr/bin/env python3
+"""Benchmark: weight-stream GB/s and us/call of the int8 decode GEMM (M <= 32), cold-L2 graph replay.
+
+Workload (default): W8A8 GEMM M=16, K=4096, N=1536 (a fused-QKV-like decode shape), int8 x_q and W
+uniform in [-127, 127], fp32 scales uniform in [1e-3, 2e-2], seeded synthetic data.  R rotating
+packed-W buffers, R = max(16, ceil(3 * L2 / W_bytes)), so every call streams its weight cold from
+HBM (inputs larger than L2; no flush needed).  One step = one CUDA-graph replay of C calls cycling
+through the R buffers.  W warm-up steps, then K timed steps bracketed by a barrier and a device
+synchronise, timed with CUDA events on the launching stream; max over ranks.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--sweep]
+Under torchrun each rank runs an independent replica (the operator has no exchange step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "weight-stream GB/s and us/call, int8 decode GEMM M<=32, cold-L2 graph replay"
+DEFAULT = dict(M=16, K=4096, N=1536, dist="uniform", seed=1)
+KERNEL_SOURCES = ["int8_weight_gemm_gb300/csrc/w8a8_gemm.cu", "int8_weight_gemm_gb300/csrc/common.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "w8a8_gemm_m16_k4096_n1536_traffic.txt")
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _kernel_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_per_launch():
+    """dram read+write bytes per launch from the committed ncu summary, if its kernel is current."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    vals = {}
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_16") != _kernel_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[2:]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands, on the host cores, on a bounded sample of the workload
+# ---------------------------------------------------------------------------------------------
+
+def cpu_baseline(M, K, N, x, xs, W, ws, budget_s=12.0, cols=None):
+    import oracle
+
+    cols = cols or N
+    Ws = np.ascontiguousarray(W[:, :cols])
+    wss = np.ascontiguousarray(ws[:cols])
+    calls = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.w8a8_gemm(x, xs, Ws, wss)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or calls >= 200:
+            break
+    per_call = el / calls
+    gbs = K * cols / per_call / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{calls} oracle calls on M={M}, K={K}, N={cols} (of {N}) columns, single thread, "
+                      f"{per_call * 1e3:.1f} ms/call"}
+
+
+# ---------------------------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------------------------
+
+def time_gemm(M, K, N, dist, seed, steps, warmup, blocks=0, device=None, sample_clocks=False, want_e2e=True,
+              flags=0):
+    import torch
+
+    import int8_weight_gemm_gb300 as lib8
+    import synth
+
+    dev = device or torch.device("cuda")
+    x, xs, W, ws = synth.w8a8_inputs(M, K, N, seed=seed, dist=dist)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20)
+    wbytes = lib8.w8a8_packed_weight_bytes(K, N)
+    R = max(16, math.ceil(3 * l2 / wbytes))
+    C = R * max(1, math.ceil(256 / R))                     # calls per graph replay
+    xd = torch.from_numpy(x).to(dev)
+    xsd = torch.from_numpy(xs).to(dev)
+    wsd = torch.from_numpy(ws).to(dev)
+    Wd = torch.from_numpy(W).to(dev)
+    wsp = lib8.alloc_workspace(lib8.w8a8_workspace_bytes(M, K, N, blocks), dev)
+    packed0 = lib8.w8a8_pack_weights(Wd, ws=wsp)
+    del Wd
+    packs = [packed0] + [packed0.clone() for _ in range(R - 1)]
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        for i in range(R):                       # eager warm-up (also loads the module)
+            lib8.w8a8_gemm(xd, xsd, packs[i], wsd, wsp, N, out=out, blocks=blocks, flags=flags, stream=stream)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for c in range(C):
+            lib8.w8a8_gemm(xd, xsd, packs[c % R], wsd, wsp, N, out=out, blocks=blocks, flags=flags, stream=stream)
+    torch.cuda.synchronize(dev)
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev.index or 0) if sample_clocks else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.15)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for i in range(steps):
+            g.replay()
+            evs[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop() if sampler else None
+    step_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
+    total_ms = evs[0].elapsed_time(evs[-1])
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    per_call_us = sorted(s * 1e3 / C for s in step_ms)
+    res = {
+        "R": R, "C": C, "wbytes": wbytes, "total_ms": total_ms, "steps": steps,
+        "us_median": statistics.median(per_call_us),
+        "us_p90": per_call_us[min(len(per_call_us) - 1, int(0.9 * len(per_call_us)))],
+        "avg_launch_us": total_ms * 1e3 / (steps * C),
+        "clocks": clocks,
+        "launches": steps * C,
+        "inputs": (x, xs, W, ws),
+    }
+    # correctness spot check of the timed configuration (first rows, against the oracle)
+    res["out"] = out
+    if want_e2e:
+        res["e2e"] = time_e2e(lib8, M, K, N, xd, xsd, packs, wsd, wsp, blocks, dev, steps=min(steps, 200), flags=flags)
+    del packs
+    return res
+
+
+def time_e2e(lib8, M, K, N, xd, xsd, packs, wsd, wsp, blocks, dev, steps, flags=0):
+    """The same call through the public API with host buffers: pinned H2D of the step's activations
+    and scales, the GEMM (cold weight), and a D2H read of the result, every step."""
+    import torch
+
+    R = len(packs)
+    xh = xd.cpu().pin_memory()
+    xsh = xsd.cpu().pin_memory()
+    outh = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for i in range(steps + 3):
+            if i == 3:
+                e0.record(stream)
+            xd.copy_(xh, non_blocking=True)
+            xsd.copy_(xsh, non_blocking=True)
+            lib8.w8a8_gemm(xd, xsd, packs[i % R], wsd, wsp, N, out=out, blocks=blocks, flags=flags, stream=stream)
+            outh.copy_(out, non_blocking=True)
+        e1.record(stream)
+    stream.synchronize()
+    per_step_us = e0.elapsed_time(e1) * 1e3 / steps
+    wbytes = lib8.w8a8_packed_weight_bytes(K, N)
+    return {"value": wbytes / per_step_us / 1e3, "unit": "GB/s", "us_per_step": per_step_us,
+            "h2d_bytes_per_step": M * K + 4 * M, "d2h_bytes_per_step": 2 * M * N}
+
+
+def time_q8(T, K, N, iters=200, seed=7, flags=0):
+    """Median us per Q8_0 read in a graph of calls over rotating weight sets (not L2-resident)."""
+    import torch
+
+    import int8_weight_gemm_gb300 as lib8
+    import synth
+
+    x, q, d = synth.q8_0_inputs(T, K, N, seed=seed)
+    props = torch.cuda.get_device_properties(0)
+    l2 = getattr(props, "L2_cache_size", 128 << 20)
+    nbytes = N * K + 2 * N * (K // 32)
+    R = max(8, math.ceil(3 * l2 / nbytes))
+    xd = x.cuda()
+    q0 = torch.from_numpy(q).cuda()
+    d0 = torch.from_numpy(d.view(np.int16)).cuda()
+    qs = [q0] + [q0.clone() for _ in range(R - 1)]
+    ds = [d0] + [d0.clone() for _ in range(R - 1)]
+    ws = lib8.alloc_workspace(lib8.q8_0_workspace_bytes(T, K, N))
+    y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for i in range(R):
+            lib8.q8_0_gemv(xd, qs[i], ds[i], ws, y=y, flags=flags, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(R):
+            lib8.q8_0_gemv(xd, qs[i], ds[i], ws, y=y, flags=flags, stream=s)
+    for _ in range(5):
+        g.replay()
+    torch.cuda.synchronize()
+    samples = []
+    for _ in range(max(10, iters // R)):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            a.record(s)
+            g.replay()
+            b.record(s)
+        s.synchronize()
+        samples.append(a.elapsed_time(b) * 1e3 / R)
+    samples.sort()
+    return {"T": T, "K": K, "N": N, "flags": flags, "us_median": statistics.median(samples),
+            "us_p90": samples[int(0.9 * (len(samples) - 1))], "weight_bytes": nbytes,
+            "GBps": nbytes / statistics.median(samples) / 1e3}
+
+
+def run_ours(args):
+    import torch
+
+    rank = _env_int("RANK", 0)
+    world = _env_int("WORLD_SIZE", 1)
+    local = _env_int("LOCAL_RANK", 0)
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    cfg = DEFAULT
+    res = time_gemm(cfg["M"], cfg["K"], cfg["N"], cfg["dist"], cfg["seed"], args.steps, args.warmup,
+                    device=dev, sample_clocks=(rank == 0))
+    M, K, N = cfg["M"], cfg["K"], cfg["N"]
+    x, xs, W, ws = res.pop("inputs")
+    wbytes = res["wbytes"]
+    total_s = res["total_ms"] / 1e3
+    value = world * wbytes * res["launches"] / total_s / 1e9
+    peak, peak_kind = _peaks()
+    alg_bytes = K * N + M * K + 4 * M + 4 * N + 2 * M * N
+    achieved = alg_bytes / (res["avg_launch_us"] * 1e-6) / 1e9
+    traffic = _traffic_per_launch()
+    out = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(res["total_ms"] / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8",
+        "data": "synthetic (seeded SplitMix64 streams; int8 U[-127,127], fp32 scales U[1e-3,2e-2])",
+        "config": {"workload": f"W8A8 GEMM M={M}, K={K}, N={N} (fused-QKV-like decode shape)",
+                   "M": M, "K": K, "N": N, "rotating_weight_buffers": res["R"], "calls_per_step": res["C"],
+                   "l2": "inputs larger than L2: each call streams a different packed W buffer "
+                         f"({res['R']} x {wbytes / 2**20:.1f} MiB rotating)",
+                   "parallelism": f"replicas x{world}"},
+        "us_per_call": {"median": round(res["us_median"], 4), "p90": round(res["us_p90"], 4)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} (copy, MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": traffic, "alg_bytes_per_launch": alg_bytes,
+                     "kernel": "w8a8_gemm_kernel<2,4,7>"},
+        "gpu_launches": res["launches"],
+        "e2e": {k: (round(v, 3) if isinstance(v, float) else v) for k, v in res["e2e"].items()},
+        "clocks": res["clocks"],
+    }
+    # one-call correctness check of the timed configuration against the oracle (first 4 rows)
+    if rank == 0:
+        import oracle
+        ref = oracle.w8a8_gemm(x[:4], xs[:4], W, ws)
+        got = res["out"][:4].cpu().view(torch.int16).numpy().view(np.uint16)
+        out["parity_rows_checked"] = int(4)
+        out["parity_mismatches"] = int(np.count_nonzero(got != ref))
+        if not args.no_q8:
+            out["q8_0"] = [time_q8(T, K8, N8) for (K8, N8) in ((4096, 320), (320, 4096)) for T in (1, 4, 6)]
+        if not args.no_cpu:
+            out["cpu_baseline"] = cpu_baseline(M, K, N, x, xs, W, ws)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_reference(args):
+    """The oracle timed on the host cores on the same metric, config and unit (a bounded sample per step)."""
+    rank = _env_int("RANK", 0)
+    if rank != 0:
+        return
+    import oracle
+    import synth
+
+    cfg = DEFAULT
+    M, K, N = cfg["M"], cfg["K"], cfg["N"]
+    x, xs, W, ws = synth.w8a8_inputs(M, K, N, seed=cfg["seed"], dist=cfg["dist"])
+    cols = 128
+    Ws = np.ascontiguousarray(W[:, :cols])
+    wss = np.ascontiguousarray(ws[:cols])
+    for _ in range(args.warmup):
+        oracle.w8a8_gemm(x, xs, Ws, wss)
+    times = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        a = time.perf_counter()
+        oracle.w8a8_gemm(x, xs, Ws, wss)
+        times.append(time.perf_counter() - a)
+    total = time.perf_counter() - t0
+    value = K * cols * args.steps / total / 1e9
+    times.sort()
+    sample = (f"each step: one oracle call on M={M}, K={K}, N={cols} columns (a slice of N={N}), "
+              "single thread, plain C")
+    out = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": _env_int("WORLD_SIZE", 1),
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total * 1e3 / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int64",
+        "data": "synthetic (seeded SplitMix64 streams; int8 U[-127,127], fp32 scales U[1e-3,2e-2])",
+        "config": {"workload": f"W8A8 GEMM M={M}, K={K}, N={N} (fused-QKV-like decode shape)", "M": M, "K": K,
+                   "N": N, "sample_columns": cols},
+        "us_per_call": {"median": round(statistics.median(times) * 1e6, 1),
+                        "p90": round(times[int(0.9 * (len(times) - 1))] * 1e6, 1)},
+        "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": sample, "value": round(value, 4), "unit": "GB/s"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(out), flush=True)
+
+
+def run_sweep(args):
+    """Every workload family (one line each, to stdout), then exit: not the contract line."""
+    import torch
+
+    rows = []
+    shapes = [(1, 512, 256, "uniform", 0), (16, 4096, 1536, "uniform", 1)]
+    shapes += [(M, K, N, "uniform", 3000 + M) for (N, K) in ((2560, 4096), (4096, 2048)) for M in (1, 4, 8, 16, 32)]
+    shapes += [(16, 4096, 24576, "mlp", 4), (16, 12288, 4096, "mlp", 4)]
+    if args.shapes:
+        shapes = [shapes[int(i)] for i in args.shapes.split(",")]
+    peak, _ = _peaks()
+    blocks_list = [int(b) for b in args.blocks.split(",")] if args.blocks else [0]
+    flags_list = [int(f) for f in args.flags.split(",")] if args.flags else [0]
+    for (M, K, N, dist, seed) in shapes:
+        for blocks, flags in [(b, f) for b in blocks_list for f in flags_list]:
+            import int8_weight_gemm_gb300 as lib8
+            slabs = lib8.w8a8_plan(M, K, N)["slabs"]
+            if blocks > slabs:
+                continue
+            r = time_gemm(M, K, N, dist, seed, args.steps, args.warmup, blocks=blocks, want_e2e=False, flags=flags)
+            gbs = r["wbytes"] / (r["us_median"] * 1e-6) / 1e9
+            row = {"M": M, "K": K, "N": N, "dist": dist, "blocks": blocks or lib8.w8a8_plan(M, K, N)["blocks"],
+                   "flags": flags,
+                   "us_median": round(r["us_median"], 3), "us_p90": round(r["us_p90"], 3),
+                   "weight_GBps": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 3), "R": r["R"]}
+            rows.append(row)
+            print(json.dumps(row), flush=True)
+            del r
+            torch.cuda.empty_cache()
+    for (K8, N8) in ((4096, 320), (320, 4096)):
+        for T in (1, 4, 6):
+            for flags in flags_list:
+                print(json.dumps(time_q8(T, K8, N8, flags=flags)), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sweep", action="store_true", help="time every workload family (extra lines)")
+    ap.add_argument("--blocks", default="", help="comma list of CTA counts for --sweep (0 = auto)")
+    ap.add_argument("--flags", default="", help="comma list of launch flags for --sweep (1 = PDL)")
+    ap.add_argument("--shapes", default="", help="comma list of sweep shape indices (default: all)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    ap.add_argument("--no-q8", action="store_true", help="skip the Q8_0 timings")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

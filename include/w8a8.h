@@ -1,0 +1,191 @@
+/*
+ * w8a8.h - C ABI of the GB300 (sm_103a) small-M quantized weight GEMM library.
+ *
+ * Two operators of an LLM serving engine's decode and speculative-verify windows:
+ *
+ *  w8a8_gemm   x_q[M,K] int8 @ W[K,N] int8 -> int32, then * x_scale[M] * w_scale[N] -> bf16[M,N],
+ *              M <= 32.  Defined by the operator line of "INT8 W8A8 GEMM - Decode (M <= 32) -
+ *              gfx928 / SGLang TP4" (header paragraph); split-K with a fused last-arrival combine
+ *              follows its section 1.1 (qkv recipe) and "Cross-shape rules that held".
+ *  q8_0_gemv   y[T,N] = x[T,K] (bf16) times Q8_0 weights (blocks of 32 int8 quants along K with one
+ *              fp16 scale each), T <= 8, bf16 out.  Defined by "sycl: STRATA_HC_Q8=1 reads the Q8_0
+ *              hyper-connection projections", section "What changed" (w = d * q, the split layout,
+ *              fixed-order partial sums, last work-group combine).
+ *
+ * Conventions for every entry point:
+ *  - Data pointers are DEVICE pointers (cudaMalloc or equivalent) unless stated otherwise; the
+ *    caller owns every buffer.  `stream` is a cudaStream_t passed as void* (NULL = legacy stream).
+ *  - Every argument check happens on the host before any launch.  A failed check launches
+ *    nothing and returns a non-zero status; nothing is thrown and nothing is printed.
+ *  - w8a8_gemm and q8_0_gemv do no host synchronisation, allocation or memset: each is exactly
+ *    one kernel launch, so a call can be captured into a CUDA graph and replayed.
+ *  - A workspace is caller-owned device memory, at least 256-byte aligned, sized with the
+ *    *_workspace_bytes queries and zeroed once with w8a8_workspace_init (outside any capture)
+ *    before its first use.  Every call leaves it ready for the next one (each arrival counter is
+ *    reset by the last arrival).  Calls that use the same workspace must not overlap in time
+ *    (use one stream per workspace); one workspace may serve both operators in turn if it is
+ *    sized for the larger of the two.
+ *  - bf16 and fp16 values are passed as their 16-bit patterns (uint16_t storage).
+ */
+#ifndef W8A8_GB300_H
+#define W8A8_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Host status codes returned by every entry point. */
+enum {
+    W8A8_OK = 0,
+    W8A8_ERR_INVALID_ARG = 1,         /* null pointer, M/T/K/N out of range, bad blocks count */
+    W8A8_ERR_UNSUPPORTED_SHAPE = 2,   /* K % 32 != 0, N % 8 != 0 (w8a8) or K % 32 != 0 (q8_0) */
+    W8A8_ERR_MISALIGNED = 3,          /* a pointer misses the alignment stated for it */
+    W8A8_ERR_WORKSPACE_TOO_SMALL = 4, /* ws_bytes below the size query's answer */
+    W8A8_ERR_CUDA = 5                 /* a CUDA runtime call failed; see w8a8_last_error() */
+};
+
+/* Device status bits, OR-ed into the first word of a workspace by a kernel that hit a fault
+ * it could survive; read back with w8a8_workspace_status.  Both leave the outputs undefined. */
+enum {
+    W8A8_DEV_WAIT_TIMEOUT = 1u,       /* a pipeline wait exceeded its bound (about one second);
+                                         the kernel abandoned the call and returned */
+    W8A8_DEV_COUNTER_CORRUPT = 2u     /* an arrival counter held a value outside [0, arrivals):
+                                         the workspace was not zeroed, or calls overlapped */
+};
+
+/* Launch flags of w8a8_gemm and q8_0_gemv. */
+enum {
+    /* Programmatic dependent launch: the kernel may become resident, and start streaming the packed
+     * weight (W_packed, or q and d of q8_0_gemv), while the work queued before it on the stream is
+     * still running; every other input, the output and the workspace are touched only after that
+     * work has completed and its memory is visible.  The caller guarantees that the weight buffers
+     * are not written by work still in flight on the stream (weights are load-time constants: pack
+     * them, then synchronise once).  Consecutive calls then overlap one call's weight prefetch with
+     * the previous call's tail, inside a CUDA graph as well. */
+    W8A8_FLAG_PDL = 1u
+};
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int w8a8_version(void);
+
+/* Static text for a host status code. */
+const char* w8a8_status_string(int status);
+
+/* Text of the last CUDA error seen by this thread inside the library ("" if none). */
+const char* w8a8_last_error(void);
+
+/* -------------------------------------------------------------------------------------------
+ * Workspaces
+ * ----------------------------------------------------------------------------------------- */
+
+/* Zero a workspace (one cudaMemsetAsync of ws_bytes on `stream`).  Call once after allocating
+ * it, before any w8a8_gemm / q8_0_gemv call that uses it and outside any stream capture; the
+ * qkv recipe of section 1.1 of the W8A8 page keeps its counters in the workspace and clears them
+ * with one async memset before the first launch.  Errors: INVALID_ARG (ws NULL or ws_bytes 0),
+ * MISALIGNED (ws not 256-byte aligned), CUDA. */
+int w8a8_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Read the device status word of a workspace into *status (0 = no device fault recorded), and
+ * clear it.  Synchronises `stream` (a host read): not for use inside a capture. */
+int w8a8_workspace_status(void* ws, size_t ws_bytes, void* stream, uint32_t* status);
+
+/* -------------------------------------------------------------------------------------------
+ * W8A8 decode GEMM
+ * ----------------------------------------------------------------------------------------- */
+
+/* Bytes of the packed weight for a [K,N] int8 W: 64 * ceil(N/64) * K. */
+size_t w8a8_packed_weight_bytes(int K, int N);
+
+/* Workspace bytes that w8a8_gemm needs for every M in [1, M_max] at this (K, N) and `blocks`
+ * (0 = the automatic plan).  Returns 0 for arguments w8a8_gemm would reject. */
+size_t w8a8_workspace_bytes(int M_max, int K, int N, int blocks);
+
+/* Pack W once, at load time and outside any timed region or capture (section 1.1 of the W8A8
+ * page, third cross-shape rule: the cold once-read weight is packed into the fragment's layout
+ * so that every fragment is one contiguous vector read).
+ *
+ *  W         [K,N] int8, row-major (W[k][n] at k*N + n), device memory.
+ *  W_packed  device buffer of w8a8_packed_weight_bytes(K, N) bytes, 16-byte aligned.  Layout,
+ *            with Np = 64*ceil(N/64), KB = K/32, g = lane/4, c = lane%4, w = j/4, b = j%4:
+ *              byte ((((t*KB + kb)*4 + s)*32 + lane)*16 + j)  for t < Np/64, kb < KB, s < 4,
+ *              lane < 32, j < 16 holds  W[k][n] XOR 0x80  (offset binary; 0x80 for n >= N) with
+ *              n = 64t + 16s + g + 8(w%2),  k = 32kb + 8c + 4(w/2) + b.
+ *            So each 64-row tile t is one contiguous run of KB 2-KiB slabs, and a CTA whose share
+ *            of the work is a run of slabs streams one contiguous byte range.
+ *  ws        optional workspace; if not NULL it is zeroed as by w8a8_workspace_init.
+ *  Requires K % 32 == 0, 1 <= K <= 65536, 1 <= N <= 1048576, N % 8 == 0.
+ *  Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA. */
+int w8a8_pack_weights(const int8_t* W, int K, int N, void* W_packed, void* ws, size_t ws_bytes,
+                      void* stream);
+
+/* out[m][n] = bf16_rne( ((float)acc[m][n] * x_scale[m]) * w_scale[n] ),
+ * acc[m][n] = sum_k x_q[m][k] * W[k][n] in exact int32.
+ *
+ *  x_q      [M,K] int8 row-major, 16-byte aligned.     x_scale  [M] fp32.
+ *  W_packed from w8a8_pack_weights(W, K, N, ...).      w_scale  [N] fp32.
+ *  out      [M,N] bf16 row-major (uint16_t storage), 16-byte aligned; rows m >= M and columns
+ *           n >= N are never written.
+ *  M in [1, 32]; K % 32 == 0; N % 8 == 0 (same limits as the pack).
+ *  blocks   number of CTAs that share the (N/64 tiles) x (K/32 blocks) work as equal contiguous
+ *           runs of 2-KiB slabs (split-K generalised: a tile's K range is cut wherever a CTA's run
+ *           starts or ends; every cut lies on a 32-aligned k).  0 = automatic (a multiple of
+ *           the SM count).  Must not exceed the number of slabs.
+ *  flags    0 or W8A8_FLAG_PDL; any other bit is INVALID_ARG.
+ *  ws       workspace of at least w8a8_workspace_bytes(M, K, N, blocks) bytes.
+ *  The int32 sums are exact (the result does not depend on `blocks`), and the epilogue order is
+ *  fixed, so the output is bit-identical for every `blocks` and every replay.
+ *  Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, WORKSPACE_TOO_SMALL, CUDA. */
+int w8a8_gemm(const int8_t* x_q, const float* x_scale, const void* W_packed, const float* w_scale,
+              void* out, int M, int K, int N, int blocks, unsigned flags, void* ws, size_t ws_bytes,
+              void* stream);
+
+/* Launch plan of a w8a8_gemm call (host-only query; launches nothing). */
+typedef struct {
+    int n8_tiles;          /* MMA column tiles of 8 covering M: 1..4 */
+    int n_tiles;           /* 64-row tiles of N */
+    int k_blocks;          /* K / 32 */
+    long long slabs;       /* n_tiles * k_blocks (2 KiB of packed weight each) */
+    int blocks;            /* CTAs launched */
+    int threads;           /* threads per CTA */
+    int stage_slabs;       /* slabs per pipeline stage */
+    int stages;            /* pipeline depth */
+    size_t smem_bytes;     /* dynamic shared memory per CTA */
+    size_t workspace_bytes;/* workspace this call needs */
+} w8a8_plan_t;
+
+int w8a8_plan(int M, int K, int N, int blocks, w8a8_plan_t* plan);
+
+/* The slab runs of a plan: bounds[i] = first slab of CTA i, bounds[blocks] = total slabs
+ * (slab u covers tile u / KB, k in [32 (u % KB), 32 (u % KB) + 32)).  n_bounds must be
+ * blocks + 1.  Host-only. */
+int w8a8_split_bounds(int K, int N, int blocks, long long* bounds, int n_bounds);
+
+/* -------------------------------------------------------------------------------------------
+ * Q8_0 weight GEMV (verify window)
+ * ----------------------------------------------------------------------------------------- */
+
+/* Workspace bytes that q8_0_gemv needs for every T in [1, T_max] at (K, N). */
+size_t q8_0_workspace_bytes(int T_max, int K, int N);
+
+/* y[t][n] = bf16_rne( sum_k x[t][k] * (d[n][k/32] * q[n][k]) ), summed in fp32 in a fixed order
+ * (bit-identical across replays).
+ *
+ *  x   [T,K] bf16 row-major, 16-byte aligned.
+ *  q   [N,K] int8 row-major: the quants of the split layout, 16-byte aligned.
+ *  d   [N,K/32] fp16 row-major: the block scales of the split layout (scale of q[n][32b..32b+31]
+ *      is d[n][b]), 2-byte aligned.
+ *  y   [T,N] bf16 row-major, 2-byte aligned; rows t >= T are never written.
+ *  T in [1, 8]; K % 32 == 0, 32 <= K <= 65536; 1 <= N <= 1048576.
+ *  flags 0 or W8A8_FLAG_PDL; any other bit is INVALID_ARG.
+ *  Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, WORKSPACE_TOO_SMALL, CUDA. */
+int q8_0_gemv(const void* x, const int8_t* q, const void* d, void* y, int T, int K, int N,
+              unsigned flags, void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W8A8_GB300_H */

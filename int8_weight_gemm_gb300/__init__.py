@@ -1,0 +1,218 @@
+"""Python binding of libw8a8_gb300.so, the GB300 small-M quantized weight GEMM library.
+
+Argument marshalling only: every function forwards to the C ABI of the same name declared in
+include/w8a8.h, passing device pointers taken from torch tensors and the current CUDA stream.
+All arithmetic runs in the library's CUDA kernels; there is no fallback path, and a missing or
+unloadable library raises at the first call.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+__all__ = [
+    "W8A8Error",
+    "lib",
+    "w8a8_version",
+    "w8a8_packed_weight_bytes",
+    "w8a8_workspace_bytes",
+    "q8_0_workspace_bytes",
+    "w8a8_workspace_init",
+    "w8a8_workspace_status",
+    "w8a8_pack_weights",
+    "w8a8_gemm",
+    "q8_0_gemv",
+    "w8a8_plan",
+    "w8a8_split_bounds",
+    "alloc_workspace",
+]
+
+W8A8_OK = 0
+W8A8_FLAG_PDL = 1
+W8A8_DEV_WAIT_TIMEOUT = 1
+W8A8_DEV_COUNTER_CORRUPT = 2
+
+# Every symbol include/w8a8.h declares, with its ctypes signature.
+_c_p = ctypes.c_void_p
+_c_i = ctypes.c_int
+_c_sz = ctypes.c_size_t
+
+
+class PlanT(ctypes.Structure):
+    _fields_ = [
+        ("n8_tiles", ctypes.c_int),
+        ("n_tiles", ctypes.c_int),
+        ("k_blocks", ctypes.c_int),
+        ("slabs", ctypes.c_longlong),
+        ("blocks", ctypes.c_int),
+        ("threads", ctypes.c_int),
+        ("stage_slabs", ctypes.c_int),
+        ("stages", ctypes.c_int),
+        ("smem_bytes", ctypes.c_size_t),
+        ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+SIGNATURES = {
+    "w8a8_version": ([], _c_i),
+    "w8a8_status_string": ([_c_i], ctypes.c_char_p),
+    "w8a8_last_error": ([], ctypes.c_char_p),
+    "w8a8_workspace_init": ([_c_p, _c_sz, _c_p], _c_i),
+    "w8a8_workspace_status": ([_c_p, _c_sz, _c_p, ctypes.POINTER(ctypes.c_uint32)], _c_i),
+    "w8a8_packed_weight_bytes": ([_c_i, _c_i], _c_sz),
+    "w8a8_workspace_bytes": ([_c_i, _c_i, _c_i, _c_i], _c_sz),
+    "w8a8_pack_weights": ([_c_p, _c_i, _c_i, _c_p, _c_p, _c_sz, _c_p], _c_i),
+    "w8a8_gemm": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_i, _c_i, _c_i, _c_i, ctypes.c_uint, _c_p, _c_sz, _c_p], _c_i),
+    "w8a8_plan": ([_c_i, _c_i, _c_i, _c_i, ctypes.POINTER(PlanT)], _c_i),
+    "w8a8_split_bounds": ([_c_i, _c_i, _c_i, ctypes.POINTER(ctypes.c_longlong), _c_i], _c_i),
+    "q8_0_workspace_bytes": ([_c_i, _c_i, _c_i], _c_sz),
+    "q8_0_gemv": ([_c_p, _c_p, _c_p, _c_p, _c_i, _c_i, _c_i, ctypes.c_uint, _c_p, _c_sz, _c_p], _c_i),
+}
+
+_lib = None
+
+
+class W8A8Error(RuntimeError):
+    def __init__(self, name, status, detail=""):
+        self.status = status
+        text = lib().w8a8_status_string(status).decode()
+        super().__init__(f"{name} failed: {text} ({status}){': ' + detail if detail else ''}")
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded C library (built in-tree on first use if absent or stale)."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        try:
+            L = ctypes.CDLL(path)
+        except OSError as e:  # no silent fallback: the CUDA path is the product
+            raise RuntimeError(f"cannot load the CUDA library {path}: {e}") from e
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def _check(name, rc):
+    if rc != W8A8_OK:
+        detail = lib().w8a8_last_error().decode()
+        raise W8A8Error(name, rc, detail)
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _nbytes(t):
+    return t.numel() * t.element_size()
+
+
+# ---------------------------------------------------------------------------------------------
+
+def w8a8_version() -> int:
+    return lib().w8a8_version()
+
+
+def w8a8_packed_weight_bytes(K: int, N: int) -> int:
+    return int(lib().w8a8_packed_weight_bytes(K, N))
+
+
+def w8a8_workspace_bytes(M_max: int, K: int, N: int, blocks: int = 0) -> int:
+    return int(lib().w8a8_workspace_bytes(M_max, K, N, blocks))
+
+
+def q8_0_workspace_bytes(T_max: int, K: int, N: int) -> int:
+    return int(lib().q8_0_workspace_bytes(T_max, K, N))
+
+
+def w8a8_plan(M: int, K: int, N: int, blocks: int = 0) -> dict:
+    p = PlanT()
+    _check("w8a8_plan", lib().w8a8_plan(M, K, N, blocks, ctypes.byref(p)))
+    return {f: getattr(p, f) for f, _ in PlanT._fields_}
+
+
+def w8a8_split_bounds(K: int, N: int, blocks: int) -> list:
+    n = blocks + 1
+    arr = (ctypes.c_longlong * n)()
+    _check("w8a8_split_bounds", lib().w8a8_split_bounds(K, N, blocks, arr, n))
+    return list(arr)
+
+
+def w8a8_workspace_init(ws, stream=None) -> None:
+    _check("w8a8_workspace_init", lib().w8a8_workspace_init(_ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def w8a8_workspace_status(ws, stream=None) -> int:
+    v = ctypes.c_uint32(0)
+    _check("w8a8_workspace_status", lib().w8a8_workspace_status(_ptr(ws), _nbytes(ws), _stream(stream), ctypes.byref(v)))
+    return int(v.value)
+
+
+def alloc_workspace(nbytes: int, device="cuda", stream=None):
+    """A zeroed workspace tensor (uint8) of at least nbytes (torch allocations are 512-B aligned)."""
+    import torch
+
+    ws = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    assert ws.data_ptr() % 256 == 0
+    w8a8_workspace_init(ws, stream)
+    return ws
+
+
+def w8a8_pack_weights(W, W_packed=None, ws=None, stream=None):
+    """Pack W [K,N] int8 (device) into the kernel layout; returns the packed uint8 tensor."""
+    import torch
+
+    K, N = W.shape
+    if W_packed is None:
+        W_packed = torch.empty(w8a8_packed_weight_bytes(K, N), dtype=torch.uint8, device=W.device)
+    rc = lib().w8a8_pack_weights(_ptr(W), K, N, _ptr(W_packed), _ptr(ws), _nbytes(ws) if ws is not None else 0,
+                                 _stream(stream))
+    _check("w8a8_pack_weights", rc)
+    return W_packed
+
+
+def w8a8_gemm(x_q, x_scale, W_packed, w_scale, ws, N: int, out=None, blocks: int = 0, flags: int = 0,
+              stream=None):
+    """out[M,N] bf16 = bf16((float(x_q @ W) * x_scale) * w_scale) through the C ABI."""
+    import torch
+
+    M, K = x_q.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x_q.device)
+    rc = lib().w8a8_gemm(_ptr(x_q), _ptr(x_scale), _ptr(W_packed), _ptr(w_scale), _ptr(out), M, K, N, blocks,
+                         flags, _ptr(ws), _nbytes(ws), _stream(stream))
+    _check("w8a8_gemm", rc)
+    return out
+
+
+def q8_0_gemv(x, q, d, ws, y=None, flags: int = 0, stream=None):
+    """y[T,N] bf16 = x[T,K] (bf16) times the Q8_0 weights (q [N,K] int8, d [N,K/32] fp16)."""
+    import torch
+
+    T, K = x.shape
+    N = q.shape[0]
+    if y is None:
+        y = torch.empty((T, N), dtype=torch.bfloat16, device=x.device)
+    rc = lib().q8_0_gemv(_ptr(x), _ptr(q), _ptr(d), _ptr(y), T, K, N, flags, _ptr(ws), _nbytes(ws),
+                         _stream(stream))
+    _check("q8_0_gemv", rc)
+    return y

@@ -1,0 +1,226 @@
+// C ABI of the library: argument checks, launch plans and error reporting.  Every check runs
+// before any launch; the compute entry points issue exactly one kernel launch and nothing else.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/w8a8.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace w8a8 {
+
+static thread_local char g_last_error[256] = "";
+
+static int cuda_fail(cudaError_t e, const char* where) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, cudaGetErrorString(e), (int)e);
+  return W8A8_ERR_CUDA;
+}
+
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Number of SMs of the current device; 152 (GB300) when no device can be queried, so that the
+// host-only plan queries answer the same way on a machine without a GPU.
+static int current_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 152;
+  }
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+    cudaGetLastError();
+    return 152;
+  }
+  return sms;
+}
+
+cudaError_t ensure_smem_attribute(const void* kernel, int bytes) {
+  // One record per (kernel, device); a small fixed table is plenty for this library's kernels.
+  struct Entry {
+    const void* k;
+    int dev;
+    int bytes;
+  };
+  static Entry table[64];
+  static int used = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (table[i].k == kernel && table[i].dev == dev && table[i].bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  if (used < 64) table[used++] = Entry{kernel, dev, bytes};
+  return cudaSuccess;
+}
+
+cudaError_t encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType type, void* base, const cuuint64_t* dims,
+                                 const cuuint64_t* strides, const cuuint32_t* box, const cuuint32_t* estr,
+                                 CUtensorMapSwizzle swizzle) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::once_flag once;
+  static cudaError_t lookup = cudaSuccess;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    void* fn = nullptr;
+    lookup = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (lookup == cudaSuccess && q != cudaDriverEntryPointSuccess) lookup = cudaErrorSymbolNotFound;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (lookup != cudaSuccess || !encode) return lookup != cudaSuccess ? lookup : cudaErrorSymbolNotFound;
+  CUresult r = encode(map, type, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace w8a8
+
+using namespace w8a8;
+
+extern "C" {
+
+int w8a8_version(void) { return 100; }
+
+const char* w8a8_status_string(int status) {
+  switch (status) {
+    case W8A8_OK: return "ok";
+    case W8A8_ERR_INVALID_ARG: return "invalid argument";
+    case W8A8_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case W8A8_ERR_MISALIGNED: return "misaligned pointer";
+    case W8A8_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case W8A8_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+const char* w8a8_last_error(void) { return g_last_error; }
+
+int w8a8_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes == 0) return W8A8_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return W8A8_ERR_MISALIGNED;
+  cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "w8a8_workspace_init");
+  return W8A8_OK;
+}
+
+int w8a8_workspace_status(void* ws, size_t ws_bytes, void* stream, uint32_t* status) {
+  if (!ws || !status || ws_bytes < kWsHeaderBytes) return W8A8_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return W8A8_ERR_MISALIGNED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, sizeof(v), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "w8a8_workspace_status");
+  *status = v;
+  return W8A8_OK;
+}
+
+size_t w8a8_packed_weight_bytes(int K, int N) {
+  if (K < 1 || N < 1) return 0;
+  return (size_t)((N + 63) / 64) * 64 * (size_t)K;
+}
+
+size_t w8a8_workspace_bytes(int M_max, int K, int N, int blocks) {
+  if (M_max < 1 || M_max > 32) return 0;
+  const int sms = current_sm_count();
+  size_t best = 0;
+  for (int m = 1; m <= M_max; m += 8) {   // one plan per n8-tile count
+    GemmPlan pl;
+    if (gemm_plan(m, K, N, blocks, sms, &pl) != W8A8_OK) return 0;
+    if (pl.workspace_bytes > best) best = pl.workspace_bytes;
+  }
+  GemmPlan pl;
+  if (gemm_plan(M_max, K, N, blocks, sms, &pl) != W8A8_OK) return 0;
+  return pl.workspace_bytes > best ? pl.workspace_bytes : best;
+}
+
+int w8a8_plan(int M, int K, int N, int blocks, w8a8_plan_t* plan) {
+  if (!plan) return W8A8_ERR_INVALID_ARG;
+  GemmPlan pl;
+  int rc = gemm_plan(M, K, N, blocks, current_sm_count(), &pl);
+  if (rc != W8A8_OK) return rc;
+  plan->n8_tiles = pl.nt8;
+  plan->n_tiles = pl.n_tiles;
+  plan->k_blocks = pl.kb;
+  plan->slabs = pl.slabs;
+  plan->blocks = pl.blocks;
+  plan->threads = pl.threads;
+  plan->stage_slabs = pl.stage_slabs;
+  plan->stages = pl.stages;
+  plan->smem_bytes = pl.smem_bytes;
+  plan->workspace_bytes = pl.workspace_bytes;
+  return W8A8_OK;
+}
+
+int w8a8_split_bounds(int K, int N, int blocks, long long* bounds, int n_bounds) {
+  if (!bounds) return W8A8_ERR_INVALID_ARG;
+  GemmPlan pl;
+  int rc = gemm_plan(1, K, N, blocks, current_sm_count(), &pl);
+  if (rc != W8A8_OK) return rc;
+  if (n_bounds != pl.blocks + 1) return W8A8_ERR_INVALID_ARG;
+  for (int i = 0; i <= pl.blocks; ++i) bounds[i] = split_lo(i, pl.slabs, pl.blocks);
+  return W8A8_OK;
+}
+
+int w8a8_pack_weights(const int8_t* W, int K, int N, void* W_packed, void* ws, size_t ws_bytes, void* stream) {
+  if (!W || !W_packed) return W8A8_ERR_INVALID_ARG;
+  if (K < 1 || K > 65536 || N < 1 || N > 1048576) return W8A8_ERR_INVALID_ARG;
+  if (K % 32 != 0 || N % 8 != 0) return W8A8_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(W_packed, 16)) return W8A8_ERR_MISALIGNED;
+  if (ws) {
+    int rc = w8a8_workspace_init(ws, ws_bytes, stream);
+    if (rc != W8A8_OK) return rc;
+  }
+  cudaError_t e = pack_launch(W, K, N, W_packed, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "w8a8_pack_weights");
+  return W8A8_OK;
+}
+
+int w8a8_gemm(const int8_t* x_q, const float* x_scale, const void* W_packed, const float* w_scale, void* out,
+              int M, int K, int N, int blocks, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
+  if (!x_q || !x_scale || !W_packed || !w_scale || !out || !ws) return W8A8_ERR_INVALID_ARG;
+  if (flags & ~(unsigned)W8A8_FLAG_PDL) return W8A8_ERR_INVALID_ARG;
+  GemmPlan pl;
+  int rc = gemm_plan(M, K, N, blocks, current_sm_count(), &pl);
+  if (rc != W8A8_OK) return rc;
+  if (!aligned(x_q, 16) || !aligned(W_packed, 16) || !aligned(out, 16) || !aligned(x_scale, 4) ||
+      !aligned(w_scale, 4) || !aligned(ws, 256))
+    return W8A8_ERR_MISALIGNED;
+  if (ws_bytes < pl.workspace_bytes) return W8A8_ERR_WORKSPACE_TOO_SMALL;
+  cudaError_t e = gemm_launch(pl, x_q, x_scale, W_packed, w_scale, out, M, K, N, ws, (flags & W8A8_FLAG_PDL) != 0,
+                              static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "w8a8_gemm");
+  return W8A8_OK;
+}
+
+size_t q8_0_workspace_bytes(int T_max, int K, int N) {
+  Q8Plan pl;
+  if (q8_plan(T_max, K, N, &pl) != W8A8_OK) return 0;
+  return pl.workspace_bytes;
+}
+
+int q8_0_gemv(const void* x, const int8_t* q, const void* d, void* y, int T, int K, int N, unsigned flags, void* ws,
+              size_t ws_bytes, void* stream) {
+  if (!x || !q || !d || !y || !ws) return W8A8_ERR_INVALID_ARG;
+  if (flags & ~(unsigned)W8A8_FLAG_PDL) return W8A8_ERR_INVALID_ARG;
+  Q8Plan pl;
+  int rc = q8_plan(T, K, N, &pl);
+  if (rc != W8A8_OK) return rc;
+  if (!aligned(x, 16) || !aligned(q, 16) || !aligned(d, 2) || !aligned(y, 2) || !aligned(ws, 256))
+    return W8A8_ERR_MISALIGNED;
+  if (ws_bytes < pl.workspace_bytes) return W8A8_ERR_WORKSPACE_TOO_SMALL;
+  cudaError_t e = q8_launch(pl, x, q, d, y, T, K, N, ws, (flags & W8A8_FLAG_PDL) != 0, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "q8_0_gemv");
+  return W8A8_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,47 @@
+// Internal host-side interfaces between the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace w8a8 {
+
+// Every workspace starts with this header; its first 32-bit word is the device status.
+constexpr size_t kWsHeaderBytes = 256;
+
+struct GemmPlan {
+  int nt8, n_tiles, kb;
+  long long slabs;
+  int blocks, threads, stage_slabs, stages;
+  size_t smem_bytes, workspace_bytes, counters_offset, partials_offset;
+};
+
+int gemm_plan(int M, int K, int N, int blocks, int sm_count, GemmPlan* plan);
+cudaError_t gemm_launch(const GemmPlan& pl, const int8_t* x, const float* xs, const void* wp, const float* wsc,
+                        void* out, int M, int K, int N, void* ws, bool pdl, cudaStream_t stream);
+cudaError_t pack_launch(const int8_t* W, int K, int N, void* out, cudaStream_t stream);
+
+struct Q8Plan {
+  int n_tiles;       // 16-row tiles of N
+  int kb;            // K / 32
+  int warps;         // warps per CTA (each a contiguous run of k blocks)
+  int splits;        // CTAs per tile along K (combined by the last arrival)
+  int blocks;        // n_tiles * splits
+  size_t workspace_bytes, counters_offset, partials_offset;
+};
+
+int q8_plan(int T, int K, int N, Q8Plan* plan);
+cudaError_t q8_launch(const Q8Plan& pl, const void* x, const int8_t* q, const void* d, void* y, int T, int K, int N,
+                      void* ws, bool pdl, cudaStream_t stream);
+
+// Encode a 2-D tiled tensor map through the driver entry point (no link-time libcuda dependency).
+cudaError_t encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType type, void* base, const cuuint64_t* dims,
+                                 const cuuint64_t* strides, const cuuint32_t* box, const cuuint32_t* estr,
+                                 CUtensorMapSwizzle swizzle);
+
+// Raise a kernel's dynamic shared memory limit once per device.
+cudaError_t ensure_smem_attribute(const void* kernel, int bytes);
+
+}  // namespace w8a8

@@ -1,0 +1,246 @@
+// Q8_0 weight GEMV for sm_103a: y[T,N] = x[T,K] (bf16) times Q8_0 weights, T <= 8, bf16 out.
+//
+// Operator: "sycl: STRATA_HC_Q8=1 reads the Q8_0 hyper-connection projections", section "What
+// changed": Q8_0 blocks of 32 int8 quants along K with one fp16 scale, the split layout (all
+// quants row-major, then all scales), fixed-order partial sums, and for the long-K shape a last
+// work-group combine through an atomic counter that never waits and is reset by the last arrival.
+//
+// GB300 mapping: one warp owns a 16-row tile of N over a contiguous run of 32-k blocks and
+// multiplies it on the bf16 tensor path (mma.sync m16n8k16): the quants convert exactly to bf16,
+// the activations are bf16 already, and the T <= 8 activation rows are the MMA's n8 columns.
+// Each block's 16x8 product is scaled by its fp16 scale d and added in fp32, block by block in
+// ascending k.  Warps of a CTA split the CTA's k range into contiguous runs and are summed in warp
+// order through shared memory; when K is long the CTAs of one tile are combined by the last to
+// arrive, in ascending split order.  Every order is fixed, so replays are bit-identical.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace w8a8 {
+
+constexpr int kQ8MaxWarps = 4;
+constexpr int kQ8MaxBlocksPerWarp = 8;
+constexpr int kQ8TargetBlocksPerWarp = 4;
+
+struct Q8Params {
+  const uint16_t* x;
+  const int8_t* q;
+  const uint16_t* d;
+  uint16_t* y;
+  uint32_t* status;
+  uint32_t* counters;
+  float4* partials;
+  int T, K, N, KB, warps, splits;
+};
+
+// Two signed int8 (bytes i0, i1 of v) -> bf16x2 (i0 in the low half), exact.  In offset binary
+// u = v ^ 0x80808080 each byte b sits in the float 2^23 + b (pattern 0x4B0000bb); subtracting
+// 2^23 + 128 leaves the int8 value, and values in [-128, 127] are exact in bf16.
+__device__ __forceinline__ uint32_t s8x2_to_bf16x2(uint32_t u, int i0, int i1) {
+  const float f0 = __int_as_float((int)__byte_perm(u, 0x4B000000u, 0x7440 + i0)) - 8388736.0f;
+  const float f1 = __int_as_float((int)__byte_perm(u, 0x4B000000u, 0x7440 + i1)) - 8388736.0f;
+  __nv_bfloat162 h = __floats2bfloat162_rn(f0, f1);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void q8_store(const Q8Params& p, const float (&v)[4], int n_a, int c) {
+  const int n_b = n_a + 8;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int t = 2 * c + (r & 1);
+    const int n = (r < 2) ? n_a : n_b;
+    if (t < p.T && n < p.N) p.y[(long long)t * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v[r]));
+  }
+}
+
+__global__ void __launch_bounds__(32 * kQ8MaxWarps) q8_0_gemv_kernel(const __grid_constant__ Q8Params p) {
+  __shared__ float4 red[kQ8MaxWarps][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int tile = blockIdx.x / p.splits;
+  const int split = blockIdx.x % p.splits;
+  const int cb0 = (int)split_lo(split, p.KB, p.splits);
+  const int cb1 = (int)split_lo(split + 1, p.KB, p.splits);
+  const int wb0 = cb0 + (int)split_lo(warp, cb1 - cb0, p.warps);
+  const int wb1 = cb0 + (int)split_lo(warp + 1, cb1 - cb0, p.warps);
+  const int nb = wb1 - wb0;
+  const int n_a = tile * 16 + g, n_b = n_a + 8;
+
+  pdl_trigger();
+  // Issue every load of this warp's run first: the read is latency-bound, not bandwidth-bound.
+  // The quants and scales are weights (never written by the work this call depends on), so they
+  // are requested before the dependency wait; the activations after it.
+  uint2 qa[kQ8MaxBlocksPerWarp], qb[kQ8MaxBlocksPerWarp];
+  uint4 xv[kQ8MaxBlocksPerWarp];
+  uint16_t da[kQ8MaxBlocksPerWarp], db[kQ8MaxBlocksPerWarp];
+#pragma unroll
+  for (int i = 0; i < kQ8MaxBlocksPerWarp; ++i) {
+    qa[i] = make_uint2(0u, 0u);
+    qb[i] = make_uint2(0u, 0u);
+    da[i] = 0;
+    db[i] = 0;
+    if (i < nb) {
+      const int kb = wb0 + i;
+      const long long k = (long long)kb * 32 + 8 * c;
+      if (n_a < p.N) {
+        qa[i] = __ldg(reinterpret_cast<const uint2*>(p.q + (long long)n_a * p.K + k));
+        da[i] = __ldg(p.d + (long long)n_a * p.KB + kb);
+      }
+      if (n_b < p.N) {
+        qb[i] = __ldg(reinterpret_cast<const uint2*>(p.q + (long long)n_b * p.K + k));
+        db[i] = __ldg(p.d + (long long)n_b * p.KB + kb);
+      }
+    }
+  }
+  pdl_wait();
+#pragma unroll
+  for (int i = 0; i < kQ8MaxBlocksPerWarp; ++i) {
+    xv[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (i < nb && g < p.T)
+      xv[i] = __ldcg(reinterpret_cast<const uint4*>(p.x + (long long)g * p.K + (long long)(wb0 + i) * 32 + 8 * c));
+  }
+
+  // One independent 16x8 block product per 32-k block (two k16 MMAs each, all step-0 MMAs issued
+  // before the step-1 ones), then the fp16 block scales applied in ascending k.
+  float blk[kQ8MaxBlocksPerWarp][4];
+  uint32_t af[kQ8MaxBlocksPerWarp][2][4];
+#pragma unroll
+  for (int i = 0; i < kQ8MaxBlocksPerWarp; ++i) {
+    blk[i][0] = blk[i][1] = blk[i][2] = blk[i][3] = 0.f;
+    const uint32_t ua0 = qa[i].x ^ 0x80808080u, ua1 = qa[i].y ^ 0x80808080u;
+    const uint32_t ub0 = qb[i].x ^ 0x80808080u, ub1 = qb[i].y ^ 0x80808080u;
+    // k 8c+0..3 (slots 2c,2c+1 <- k 8c,8c+1; slots 2c+8,2c+9 <- k 8c+2,8c+3), then k 8c+4..7
+    af[i][0][0] = s8x2_to_bf16x2(ua0, 0, 1);
+    af[i][0][1] = s8x2_to_bf16x2(ub0, 0, 1);
+    af[i][0][2] = s8x2_to_bf16x2(ua0, 2, 3);
+    af[i][0][3] = s8x2_to_bf16x2(ub0, 2, 3);
+    af[i][1][0] = s8x2_to_bf16x2(ua1, 0, 1);
+    af[i][1][1] = s8x2_to_bf16x2(ub1, 0, 1);
+    af[i][1][2] = s8x2_to_bf16x2(ua1, 2, 3);
+    af[i][1][3] = s8x2_to_bf16x2(ub1, 2, 3);
+  }
+#pragma unroll
+  for (int st = 0; st < 2; ++st)
+#pragma unroll
+    for (int i = 0; i < kQ8MaxBlocksPerWarp; ++i)
+      if (i < nb)
+        mma_bf16_16816(blk[i], af[i][st][0], af[i][st][1], af[i][st][2], af[i][st][3], st ? xv[i].z : xv[i].x,
+                       st ? xv[i].w : xv[i].y);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < kQ8MaxBlocksPerWarp; ++i) {
+    if (i < nb) {
+      const float sa = __half2float(__ushort_as_half(da[i]));
+      const float sb = __half2float(__ushort_as_half(db[i]));
+      acc[0] = fmaf(sa, blk[i][0], acc[0]);
+      acc[1] = fmaf(sa, blk[i][1], acc[1]);
+      acc[2] = fmaf(sb, blk[i][2], acc[2]);
+      acc[3] = fmaf(sb, blk[i][3], acc[3]);
+    }
+  }
+
+  red[warp][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  __syncthreads();
+  if (warp != 0) return;
+  float tot[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int w = 0; w < p.warps; ++w) {
+    const float4 v = red[w][lane];
+    tot[0] += v.x;
+    tot[1] += v.y;
+    tot[2] += v.z;
+    tot[3] += v.w;
+  }
+  if (p.splits == 1) {
+    q8_store(p, tot, n_a, c);
+    return;
+  }
+  float4* mine = p.partials + ((long long)tile * p.splits + split) * 32;
+  __stcg(mine + lane, make_float4(tot[0], tot[1], tot[2], tot[3]));
+  __threadfence();
+  __syncwarp();
+  uint32_t old = 0;
+  if (lane == 0) old = atomicAdd(p.counters + tile, 1u);
+  old = __shfl_sync(0xffffffffu, old, 0);
+  if (old >= (uint32_t)p.splits) {
+    if (lane == 0) atomicOr(p.status, W8A8_DEV_COUNTER_CORRUPT);
+    return;
+  }
+  if (old != (uint32_t)p.splits - 1) return;
+  __threadfence();
+  // Ascending split order; each batch's loads are all in flight before the first is used.
+  float sum[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int base = 0; base < p.splits; base += 8) {
+    float4 v[8];
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const int s = base + b;
+      v[b] = make_float4(tot[0], tot[1], tot[2], tot[3]);
+      if (s < p.splits && s != split) v[b] = __ldcg(p.partials + ((long long)tile * p.splits + s) * 32 + lane);
+    }
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      if (base + b < p.splits) {
+        sum[0] += v[b].x;
+        sum[1] += v[b].y;
+        sum[2] += v[b].z;
+        sum[3] += v[b].w;
+      }
+    }
+  }
+  if (lane == 0) atomicExch(p.counters + tile, 0u);
+  q8_store(p, sum, n_a, c);
+}
+
+int q8_plan(int T, int K, int N, Q8Plan* plan) {
+  if (T < 1 || T > 8 || K < 1 || K > 65536 || N < 1 || N > 1048576) return W8A8_ERR_INVALID_ARG;
+  if (K % 32 != 0) return W8A8_ERR_UNSUPPORTED_SHAPE;
+  Q8Plan pl{};
+  pl.n_tiles = (N + 15) / 16;
+  pl.kb = K / 32;
+  int warps = (pl.kb + kQ8TargetBlocksPerWarp - 1) / kQ8TargetBlocksPerWarp;
+  pl.warps = warps < kQ8MaxWarps ? warps : kQ8MaxWarps;
+  const int per_cta = pl.warps * kQ8TargetBlocksPerWarp;
+  pl.splits = (pl.kb + per_cta - 1) / per_cta;
+  pl.blocks = pl.n_tiles * pl.splits;
+  const size_t counters = ((size_t)pl.n_tiles * 4 + 255) / 256 * 256;
+  const size_t partials = pl.splits > 1 ? (size_t)pl.n_tiles * pl.splits * 32 * 16 : 0;
+  pl.counters_offset = kWsHeaderBytes;
+  pl.partials_offset = kWsHeaderBytes + counters;
+  pl.workspace_bytes = kWsHeaderBytes + counters + partials;
+  *plan = pl;
+  return W8A8_OK;
+}
+
+cudaError_t q8_launch(const Q8Plan& pl, const void* x, const int8_t* q, const void* d, void* y, int T, int K, int N,
+                      void* ws, bool pdl, cudaStream_t stream) {
+  Q8Params p;
+  p.x = static_cast<const uint16_t*>(x);
+  p.q = q;
+  p.d = static_cast<const uint16_t*>(d);
+  p.y = static_cast<uint16_t*>(y);
+  p.status = static_cast<uint32_t*>(ws);
+  p.counters = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + pl.counters_offset);
+  p.partials = reinterpret_cast<float4*>(static_cast<uint8_t*>(ws) + pl.partials_offset);
+  p.T = T;
+  p.K = K;
+  p.N = N;
+  p.KB = pl.kb;
+  p.warps = pl.warps;
+  p.splits = pl.splits;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)pl.blocks);
+  cfg.blockDim = dim3((unsigned)(32 * pl.warps));
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, q8_0_gemv_kernel, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace w8a8

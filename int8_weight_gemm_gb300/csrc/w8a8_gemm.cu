@@ -1,0 +1,510 @@
+// W8A8 decode GEMM for sm_103a: out[M,N] = bf16((float(x_q @ W) * x_scale) * w_scale), M <= 32.
+//
+// Operator: "INT8 W8A8 GEMM - Decode (M <= 32) - gfx928 / SGLang TP4", header paragraph.
+// Structure follows that page's section 1.1 recipes and cross-shape rules, re-planned for GB300:
+//  * the weight is packed once into the fragment layout (third cross-shape rule) so that the
+//    kernel streams it as one contiguous byte range per CTA;
+//  * split-K over a CTA count tied to the SM count (first rule), generalised to equal runs of
+//    2 KiB slabs over the linearised (tile, k-block) space, all cuts on 32-aligned k;
+//  * a fused last-arrival combine (qkv recipe: counter per output tile, fence + atomic, the last
+//    arriver sums the partials in ascending order, scales and stores bf16) in one launch;
+//  * exact int32 sums, k-ascending within a split and ascending over splits.
+//
+// GB300 choices (prior art on the pages is gfx928 DUMMA; none of it carries over literally):
+//  * The weight stream goes HBM -> shared memory through the TMA engine (cp.async.bulk, 1-D,
+//    evict-first L2 policy) into an NS-deep ring of stages, issued by one producer warp.
+//  * int8 tensor-core throughput on this part is far below what a weight stream at HBM speed
+//    needs at M = 16 (measured: mma.sync s8 ~150 TOPS vs fp16 ~600 TFLOPS), so the int8 values
+//    are converted exactly to fp16 (every int8 is an fp16 integer) and multiplied on the fp16
+//    tensor path with fp32 accumulation.  Products are integers of magnitude <= 2^14 and a
+//    partial sum over at most 512 k stays <= 2^23, so every fp32 accumulator value is an exact
+//    integer; the fp32 partials are converted to int32 (exactly) at least every 512 k and summed
+//    in int32.  The result is the int32 sum an int8 MMA would produce, bit for bit.
+//  * Weight rows are the MMA's M dimension (16 rows per warp) and the activation rows are its
+//    N dimension (n8 tiles), so M <= 8 wastes nothing on a 16-row MMA tile.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace w8a8 {
+
+constexpr int kTileRows = 64;                      // rows of N per tile
+constexpr int kKBlock = 32;                        // k per slab
+constexpr int kSlabBytes = kTileRows * kKBlock;    // 2048
+constexpr int kConsumerWarps = 8;                  // two per stage slot: even / odd stages
+constexpr int kWarpsPerStage = 4;                  // one slab of a stage each
+constexpr int kSubTiles = 4;                       // 16-row sub-tiles of a 64-row tile
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kFlushSlabs = 16;                    // 16 slabs of 32 k = 512 k per warp between int32 flushes
+
+constexpr int kStageSlabs = 4;                     // one slab per consumer warp per stage
+
+template <int NT8, int NS>
+struct GemmLayout {
+  static_assert(kStageSlabs * kKBlock == 128, "the activation box row is one 128-byte swizzle span");
+  static constexpr int kXRows = 8 * NT8;                    // activation rows loaded (zero past M)
+  static constexpr int kXRawStage = kXRows * 128;           // raw int8 box, 128B-swizzled, 1 KiB multiple
+  static constexpr int kWStage = kStageSlabs * kSlabBytes;
+  static constexpr int kSegSumInts = 2 * 4 * NT8 * 32 * 4;  // two int32 [sub][j][lane][4] segment sums
+  static constexpr int kBytes = 1024 + NS * (kXRawStage + kWStage) + kSegSumInts * 4;   // + alignment slack
+};
+
+// --------------------------------------------------------------------------------------------
+// Pack: W[K,N] row-major int8 -> packed slabs (layout documented in w8a8.h).
+// --------------------------------------------------------------------------------------------
+__global__ void w8a8_pack_kernel(const int8_t* __restrict__ W, int K, int N, int KB, long long chunks,
+                                 uint4* __restrict__ out) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < chunks; idx += stride) {
+    const int lane = (int)(idx & 31);
+    long long r = idx >> 5;
+    const int s = (int)(r & 3);
+    r >>= 2;
+    const int kb = (int)(r % KB);
+    const long long t = r / KB;
+    const int g = lane >> 2, c = lane & 3;
+    uint32_t words[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const long long n = 64 * t + 16 * s + g + 8 * (w & 1);
+      const int kbase = 32 * kb + 8 * c + 4 * (w >> 1);
+      uint32_t v = 0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const uint32_t byte = n < N ? (uint32_t)(uint8_t)W[(long long)(kbase + b) * N + n] ^ 0x80u : 0x80u;
+        v |= byte << (8 * b);
+      }
+      words[w] = v;
+    }
+    out[idx] = make_uint4(words[0], words[1], words[2], words[3]);
+  }
+}
+
+// --------------------------------------------------------------------------------------------
+// GEMM
+// --------------------------------------------------------------------------------------------
+struct GemmParams {
+  CUtensorMap xmap;   // x_q [M, K] int8, box 128 x (8 * NT8), 128-byte swizzle, zero fill past M
+  const uint8_t* wp;
+  const float* x_scale;
+  const float* w_scale;
+  uint16_t* out;
+  uint32_t* status;
+  uint32_t* counters;
+  int4* tile_acc;     // per 16-row sub-tile: int32 accumulator of split tiles, zero between calls
+  int M, K, N, KB;
+  long long U;
+  int G;
+  int pdl;            // launched with programmatic dependent launch: prefetch W before the wait
+};
+
+// Walks a CTA's run of slabs [b0, b1) as stages of at most SS slabs that never cross a tile.
+struct StageIter {
+  long long u, b1, seg_begin, seg_end, t;
+  int KB, ns, ss;
+  __device__ StageIter(long long b0_, long long b1_, int KB_, int ss_) : u(b0_), b1(b1_), KB(KB_), ss(ss_) {
+    begin_segment();
+  }
+  __device__ void begin_segment() {
+    t = u / KB;
+    seg_begin = u;
+    seg_end = min(b1, (t + 1) * (long long)KB);
+    ns = (int)min((long long)ss, seg_end - u);
+  }
+  __device__ bool done() const { return u >= b1; }
+  __device__ int kb0() const { return (int)(u - t * KB); }
+  __device__ bool last_of_segment() const { return u + ns >= seg_end; }
+  __device__ void next() {
+    u += ns;
+    if (u >= b1) return;
+    if (u >= seg_end) begin_segment();
+    else ns = (int)min((long long)ss, seg_end - u);
+  }
+};
+
+// out[m][n] for this lane's accumulator fragment: (row g / g+8 of the sub-tile) x (columns
+// 2c, 2c+1 of each n8 tile).  xs holds x_scale of the lane's columns, wsc w_scale of its rows.
+template <int NT8>
+__device__ __forceinline__ void store_epilogue(const GemmParams& p, const int (&v)[NT8][4], const float (&xs)[NT8][2],
+                                               const float (&wsc)[2], int n0, int g, int c) {
+#pragma unroll
+  for (int j = 0; j < NT8; ++j) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int m = 8 * j + 2 * c + (r & 1);
+      const int n = n0 + g + 8 * (r >> 1);
+      if (m < p.M && n < p.N) {
+        float f = __int2float_rn(v[j][r]);
+        f = __fmul_rn(f, xs[j][r & 1]);
+        f = __fmul_rn(f, wsc[r >> 1]);
+        p.out[(long long)m * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(f));
+      }
+    }
+  }
+}
+
+template <int NT8, int NS>
+__global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_constant__ GemmParams p) {
+  using L = GemmLayout<NT8, NS>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[NS];   // W slabs + raw activation box of a stage landed
+  __shared__ __align__(8) uint64_t empty_bar[NS];  // the stage's consumer warps took their slabs
+  __shared__ __align__(8) uint64_t seg_bar;        // all consumer threads added a segment's sums
+  __shared__ int abort_flag;
+
+  // 128B-swizzled TMA boxes need a 1 KiB aligned destination.
+  uint8_t* const smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* const xraw = smem;
+  uint8_t* const wring = xraw + NS * L::kXRawStage;
+  int* const segsum = reinterpret_cast<int*>(wring + NS * L::kWStage);   // [2][sub][j][lane][4] int32
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kWarpsPerStage);
+    }
+    mbar_init(&seg_bar, 32 * kConsumerWarps);
+    abort_flag = 0;
+    mbar_fence_init();
+  }
+  for (int i = threadIdx.x; i < L::kSegSumInts; i += kThreads) segsum[i] = 0;
+  __syncthreads();
+  pdl_trigger();   // the next call on the stream may start its own weight prefetch
+
+  const long long b0 = split_lo(blockIdx.x, p.U, p.G);
+  const long long b1 = split_lo(blockIdx.x + 1, p.U, p.G);
+
+  if (warp == kConsumerWarps) {
+    // ---------------------------------------------------------------- producer (one thread)
+    if (lane != 0) return;
+    tma_prefetch_desc(&p.xmap);
+    const uint64_t policy = policy_evict_first();
+    const uint32_t xbox = (uint32_t)L::kXRawStage;
+    StageIter it(b0, b1, p.KB, kStageSlabs);
+    int q = 0;
+    if (p.pdl) {
+      // The packed weight is never written by the work this call depends on: start streaming it
+      // before the dependency wait, then add the activation boxes once the wait has returned.
+      StageIter pre = it;
+      int npre = 0;
+      while (npre < NS && !pre.done()) {
+        mbar_arrive_expect_tx(&full_bar[npre], (uint32_t)(pre.ns * kSlabBytes) + xbox);
+        bulk_g2s_hint(wring + npre * L::kWStage, p.wp + pre.u * kSlabBytes, (uint32_t)(pre.ns * kSlabBytes),
+                      &full_bar[npre], policy);
+        pre.next();
+        ++npre;
+      }
+      pdl_wait();
+      for (; q < npre; ++q, it.next())
+        tma_load_2d(xraw + q * L::kXRawStage, &p.xmap, it.kb0() * kKBlock, 0, &full_bar[q]);
+    } else {
+      pdl_wait();
+    }
+    for (; !it.done(); it.next(), ++q) {
+      const int s = q % NS;
+      if (q >= NS && !mbar_wait(&empty_bar[s], ((q / NS) & 1) ^ 1, &abort_flag, p.status)) break;
+      mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(it.ns * kSlabBytes) + xbox);
+      bulk_g2s_hint(wring + s * L::kWStage, p.wp + it.u * kSlabBytes, (uint32_t)(it.ns * kSlabBytes), &full_bar[s],
+                    policy);
+      tma_load_2d(xraw + s * L::kXRawStage, &p.xmap, it.kb0() * kKBlock, 0, &full_bar[s]);
+    }
+    // Drain: every copy this thread issued must land before the CTA may exit.
+    for (int s = 0; s < NS && s < q; ++s) {
+      const int last = s + NS * ((q - 1 - s) / NS);
+      mbar_wait_drain(&full_bar[s], (uint32_t)((last / NS) & 1), p.status);
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- consumer warps
+  // Warp w multiplies slab (w % 4) of every stage of parity (w / 4), covering all four 16-row
+  // sub-tiles of the 64-row tile.  Each warp converts only its own 32-k activation slice, so the
+  // warps never wait for one another inside a tile.  Their fp32 partials (exact integers) are
+  // flushed as int32 into a shared per-segment sum; warps 0..3 finish sub-tiles 0..3.
+  pdl_wait();
+  const int g = lane >> 2, c = lane & 3;
+  const int slab = warp & (kStageSlabs - 1);
+  const int parity = warp / kStageSlabs;
+  float xs[NT8][2];
+  float wsc[2] = {0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < NT8; ++j)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int m = 8 * j + 2 * c + e;
+      xs[j][e] = (warp < 4 && m < p.M) ? __ldg(p.x_scale + m) : 0.f;
+    }
+  float facc[4][NT8][4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int j = 0; j < NT8; ++j)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) facc[u][j][r] = 0.f;
+  int since = 0;   // slabs accumulated in fp32 by this warp since its last flush
+  int segs = 0;
+  int q = 0;
+
+  // Add this warp's fp32 partial sums (exact integers) into the segment's shared int32 sums.
+  auto flush = [&](int* dst) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int j = 0; j < NT8; ++j)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int v = __float2int_rn(facc[u][j][r]);
+          if (v != 0) atomicAdd(dst + ((u * NT8 + j) * 32 + lane) * 4 + r, v);
+          facc[u][j][r] = 0.f;
+        }
+  };
+
+  for (StageIter it(b0, b1, p.KB, kStageSlabs); !it.done(); it.next(), ++q) {
+    const int s = q % NS;
+    if (it.u == it.seg_begin && warp < 4) {
+      // Start of a tile segment: fetch the w_scale values this warp's epilogue will need now, so
+      // that their latency hides behind the segment's stream.
+      const int nr = (int)(it.t * kTileRows) + 16 * warp + g;
+      wsc[0] = nr < p.N ? __ldg(p.w_scale + nr) : 0.f;
+      wsc[1] = nr + 8 < p.N ? __ldg(p.w_scale + nr + 8) : 0.f;
+    }
+    if ((q & 1) == parity) {
+      if (!mbar_wait(&full_bar[s], (uint32_t)((q / NS) & 1), &abort_flag, p.status)) return;
+      if (slab < it.ns) {
+        // Weight fragments of the four sub-tiles, then this slab's activation B fragments.
+        const uint8_t* wst = wring + s * L::kWStage + slab * kSlabBytes + lane * 16;
+        uint4 w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) w[u] = *reinterpret_cast<const uint4*>(wst + u * 512);
+        // Row m of the box sits at m * 128 with its 16-byte chunks XOR-swizzled by (m & 7) = g.
+        const uint8_t* xr = xraw + s * L::kXRawStage;
+        const int chunk = 2 * slab + (c >> 1);
+        uint32_t b[NT8][4];
+#pragma unroll
+        for (int j = 0; j < NT8; ++j) {
+          const uint2 v = *reinterpret_cast<const uint2*>(xr + (8 * j + g) * 128 + ((chunk ^ g) << 4) + 8 * (c & 1));
+          offset_bytes_to_half2(v.x ^ 0x80808080u, b[j][0], b[j][1]);
+          offset_bytes_to_half2(v.y ^ 0x80808080u, b[j][2], b[j][3]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);   // registers hold everything this warp needs
+        if (since == kFlushSlabs) {
+          flush(segsum + (segs & 1) * L::kSegSumInts / 2);
+          since = 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint32_t a[2][4];
+          offset_bytes_to_half2(w[u].x, a[0][0], a[0][2]);   // row g,   k 8c+0..3
+          offset_bytes_to_half2(w[u].y, a[0][1], a[0][3]);   // row g+8, k 8c+0..3
+          offset_bytes_to_half2(w[u].z, a[1][0], a[1][2]);   // row g,   k 8c+4..7
+          offset_bytes_to_half2(w[u].w, a[1][1], a[1][3]);   // row g+8, k 8c+4..7
+#pragma unroll
+          for (int st = 0; st < 2; ++st)
+#pragma unroll
+            for (int j = 0; j < NT8; ++j)
+              mma_f16_16816(facc[u][j], a[st][0], a[st][1], a[st][2], a[st][3], b[j][2 * st], b[j][2 * st + 1]);
+        }
+        ++since;
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+      }
+    }
+    if (!it.last_of_segment()) continue;
+
+    // ------------------------------------------------------------ end of this CTA's part of a tile
+    int* const sums = segsum + (segs & 1) * L::kSegSumInts / 2;
+    if (since) flush(sums);
+    since = 0;
+    mbar_arrive(&seg_bar);
+    if (!mbar_wait(&seg_bar, (uint32_t)(segs & 1), &abort_flag, p.status)) return;
+    ++segs;
+    if (warp >= 4) continue;
+    // Warp `sub` takes sub-tile `sub` of the segment's sums and clears them for segment segs + 1
+    // (the next user of this buffer waits on a later segment barrier, which these warps reach
+    // only after the clear).
+    const int sub = warp;
+    int part[NT8][4];
+#pragma unroll
+    for (int j = 0; j < NT8; ++j) {
+      int4* cell = reinterpret_cast<int4*>(sums) + (sub * NT8 + j) * 32 + lane;
+      const int4 v = *cell;
+      part[j][0] = v.x;
+      part[j][1] = v.y;
+      part[j][2] = v.z;
+      part[j][3] = v.w;
+      *cell = make_int4(0, 0, 0, 0);
+    }
+    const long long t = it.t;
+    const int n0 = (int)(t * kTileRows) + 16 * sub;
+    if (it.seg_begin == t * p.KB && it.seg_end == (t + 1) * p.KB) {   // the whole tile is ours
+      store_epilogue<NT8>(p, part, xs, wsc, n0, g, c);
+      continue;
+    }
+    // Split tile (qkv recipe's fused tail): add the int32 partial into the tile's accumulator in
+    // the workspace, make it visible GPU-wide, then count the arrival.  int32 addition is
+    // associative, so the total is the same bits as an ascending-order sum of the partials.  The
+    // last arrival reads the total (its own partial included), returns the accumulator and the
+    // counter to zero for the next call, and stores the bf16 tile.
+    int* tacc = reinterpret_cast<int*>(p.tile_acc + (t * kSubTiles + sub) * (NT8 * 32)) + lane * 4;
+#pragma unroll
+    for (int j = 0; j < NT8; ++j)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) red_add_s32(tacc + j * 128 + r, part[j][r]);
+    __threadfence();
+    __syncwarp();
+    const long long i_lo = split_owner(t * p.KB, p.U, p.G);
+    const long long i_hi = split_owner((t + 1) * p.KB - 1, p.U, p.G);
+    const uint32_t arrivals = (uint32_t)(i_hi - i_lo + 1);
+    uint32_t* ctr = p.counters + t * kSubTiles + sub;
+    uint32_t old = 0;
+    if (lane == 0) old = atom_add_acq_rel_u32(ctr, 1u);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old >= arrivals) {
+      if (lane == 0) atomicOr(p.status, W8A8_DEV_COUNTER_CORRUPT);
+      continue;
+    }
+    if (old != arrivals - 1) continue;
+    __syncwarp();
+    __threadfence();
+    int tot[NT8][4];
+#pragma unroll
+    for (int j = 0; j < NT8; ++j) {
+      const int4 v = __ldcg(reinterpret_cast<const int4*>(tacc + j * 128));
+      tot[j][0] = v.x;
+      tot[j][1] = v.y;
+      tot[j][2] = v.z;
+      tot[j][3] = v.w;
+    }
+#pragma unroll
+    for (int j = 0; j < NT8; ++j) __stcg(reinterpret_cast<int4*>(tacc + j * 128), make_int4(0, 0, 0, 0));
+    if (lane == 0) *reinterpret_cast<volatile uint32_t*>(ctr) = 0u;
+    store_epilogue<NT8>(p, tot, xs, wsc, n0, g, c);
+  }
+}
+
+// --------------------------------------------------------------------------------------------
+// Host side
+// --------------------------------------------------------------------------------------------
+// Pipeline depth per n8-tile count, sized for two CTAs per SM.
+constexpr int kStages1 = 10, kStages2 = 9, kStages3 = 8, kStages4 = 7;
+
+static int gemm_stages(int nt8) {
+  switch (nt8) {
+    case 1: return kStages1;
+    case 2: return kStages2;
+    case 3: return kStages3;
+    default: return kStages4;
+  }
+}
+
+static size_t gemm_smem_bytes(int nt8) {
+  switch (nt8) {
+    case 1: return GemmLayout<1, kStages1>::kBytes;
+    case 2: return GemmLayout<2, kStages2>::kBytes;
+    case 3: return GemmLayout<3, kStages3>::kBytes;
+    default: return GemmLayout<4, kStages4>::kBytes;
+  }
+}
+
+static constexpr int kAutoCtasPerSm = 2;
+
+int gemm_plan(int M, int K, int N, int blocks, int sm_count, GemmPlan* plan) {
+  if (M < 1 || M > 32 || K < 1 || K > 65536 || N < 1 || N > 1048576 || blocks < 0) return W8A8_ERR_INVALID_ARG;
+  if (K % 32 != 0 || N % 8 != 0) return W8A8_ERR_UNSUPPORTED_SHAPE;
+  GemmPlan pl{};
+  pl.nt8 = (M + 7) / 8;
+  pl.n_tiles = (N + kTileRows - 1) / kTileRows;
+  pl.kb = K / kKBlock;
+  pl.slabs = (long long)pl.n_tiles * pl.kb;
+  if (blocks == 0) {
+    long long g = (long long)kAutoCtasPerSm * (sm_count > 0 ? sm_count : 152);
+    pl.blocks = (int)(g < pl.slabs ? g : pl.slabs);
+  } else {
+    if (blocks > pl.slabs) return W8A8_ERR_INVALID_ARG;
+    pl.blocks = blocks;
+  }
+  pl.threads = kThreads;
+  pl.stage_slabs = kStageSlabs;
+  pl.stages = gemm_stages(pl.nt8);
+  pl.smem_bytes = gemm_smem_bytes(pl.nt8);
+  const size_t counters = ((size_t)pl.n_tiles * kSubTiles * 4 + 255) / 256 * 256;
+  const size_t partials = (size_t)pl.n_tiles * kSubTiles * pl.nt8 * 32 * 16;   // tile accumulators
+  pl.counters_offset = kWsHeaderBytes;
+  pl.partials_offset = kWsHeaderBytes + counters;
+  pl.workspace_bytes = kWsHeaderBytes + counters + partials;
+  *plan = pl;
+  return W8A8_OK;
+}
+
+template <int NT8, int NS>
+static cudaError_t launch_gemm(const GemmParams& p, int blocks, bool pdl, cudaStream_t stream) {
+  auto kern = w8a8_gemm_kernel<NT8, NS>;
+  const int smem = GemmLayout<NT8, NS>::kBytes;
+  cudaError_t e = ensure_smem_attribute((const void*)kern, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t gemm_launch(const GemmPlan& pl, const int8_t* x, const float* xs, const void* wp, const float* wsc,
+                        void* out, int M, int K, int N, void* ws, bool pdl, cudaStream_t stream) {
+  GemmParams p;
+  // Activation tensor map: [M rows, K bytes], box of 128 bytes x 8*NT8 rows (rows >= M read as 0).
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)K};
+  const cuuint32_t box[2] = {128u, (cuuint32_t)(8 * pl.nt8)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  cudaError_t e = encode_tensor_map_2d(&p.xmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<int8_t*>(x), dims, strides,
+                                       box, estr, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  p.wp = static_cast<const uint8_t*>(wp);
+  p.x_scale = xs;
+  p.w_scale = wsc;
+  p.out = static_cast<uint16_t*>(out);
+  p.status = static_cast<uint32_t*>(ws);
+  p.counters = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + pl.counters_offset);
+  p.tile_acc = reinterpret_cast<int4*>(static_cast<uint8_t*>(ws) + pl.partials_offset);
+  p.M = M;
+  p.K = K;
+  p.N = N;
+  p.KB = pl.kb;
+  p.U = pl.slabs;
+  p.G = pl.blocks;
+  p.pdl = pdl ? 1 : 0;
+  switch (pl.nt8) {
+    case 1: return launch_gemm<1, kStages1>(p, pl.blocks, pdl, stream);
+    case 2: return launch_gemm<2, kStages2>(p, pl.blocks, pdl, stream);
+    case 3: return launch_gemm<3, kStages3>(p, pl.blocks, pdl, stream);
+    default: return launch_gemm<4, kStages4>(p, pl.blocks, pdl, stream);
+  }
+}
+
+cudaError_t pack_launch(const int8_t* W, int K, int N, void* out, cudaStream_t stream) {
+  const int KB = K / kKBlock;
+  const long long tiles = (N + kTileRows - 1) / kTileRows;
+  const long long chunks = tiles * KB * 4 * 32;
+  long long grid = (chunks + 255) / 256;
+  if (grid > 65535) grid = 65535;
+  w8a8_pack_kernel<<<(unsigned)grid, 256, 0, stream>>>(W, K, N, KB, chunks, static_cast<uint4*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace w8a8

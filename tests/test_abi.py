@@ -1,0 +1,182 @@
+"""CPU tests of the C-ABI library: it loads, exports every symbol include/w8a8.h declares, and its
+host-only logic (sizes, plans, split bounds, argument checks) is right.  No kernel runs here."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import int8_weight_gemm_gb300 as lib8
+import oracle
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w8a8.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if not n.startswith("W8A8_GB300")))
+
+
+def test_header_declares_the_expected_entry_points():
+    names = _declared_functions()
+    for required in ("w8a8_pack_weights", "w8a8_gemm", "q8_0_gemv"):
+        assert required in names
+    assert set(names) == set(lib8.SIGNATURES), (set(names) ^ set(lib8.SIGNATURES))
+
+
+def test_library_exports_every_declared_symbol():
+    L = lib8.lib()
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_version_and_status_strings():
+    assert lib8.w8a8_version() >= 100
+    assert lib8.lib().w8a8_status_string(0) == b"ok"
+    assert lib8.lib().w8a8_status_string(4) == b"workspace too small"
+
+
+@pytest.mark.parametrize("K,N", [(512, 256), (4096, 1536), (32, 8), (96, 200), (12288, 4096)])
+def test_packed_bytes_match_oracle_layout(K, N):
+    assert lib8.w8a8_packed_weight_bytes(K, N) == oracle.w8a8_packed_bytes(K, N)
+
+
+@pytest.mark.parametrize("K,N,blocks", [(512, 256, 0), (4096, 1536, 0), (4096, 1536, 7), (4096, 24576, 0),
+                                        (64, 200, 0), (64, 200, 8), (12288, 4096, 304), (32, 8, 1)])
+def test_split_bounds_cover_every_slab_once(K, N, blocks):
+    plan = lib8.w8a8_plan(1, K, N, blocks)
+    G, U, KB = plan["blocks"], plan["slabs"], plan["k_blocks"]
+    assert U == -(-N // 64) * (K // 32) and KB == K // 32
+    b = lib8.w8a8_split_bounds(K, N, G)
+    assert b[0] == 0 and b[-1] == U and len(b) == G + 1
+    sizes = np.diff(b)
+    assert (sizes >= 1).all()                         # no empty run (the combine relies on it)
+    assert sizes.max() - sizes.min() <= 1             # equal runs to within one slab
+    # Brute force: contributors of each tile from the runs, against the owner arithmetic the
+    # kernel uses (first CTA of the tile's first slab .. CTA of its last slab).
+    owner = np.searchsorted(np.array(b[1:]), np.arange(U), side="right")
+    for t in range(U // KB):
+        contrib = sorted(set(owner[t * KB:(t + 1) * KB].tolist()))
+        assert contrib == list(range(contrib[0], contrib[-1] + 1))
+        lo = ((t * KB + 1) * G + U - 1) // U - 1
+        hi = (((t + 1) * KB) * G + U - 1) // U - 1
+        assert (lo, hi) == (contrib[0], contrib[-1])
+
+
+def test_split_slices_reproduce_the_oracle_sums():
+    # Host replay of the plan: summing each CTA's k-slices of every tile in int32, in ascending CTA
+    # order, must give the oracle's sums (the invariant behind the combine).
+    M, K, N, G = 3, 256, 128, 5
+    x, _, W, _ = synth.w8a8_inputs(M, K, N, seed=4)
+    ref = oracle.w8a8_acc(x, W)
+    b = lib8.w8a8_split_bounds(K, N, G)
+    KB = K // 32
+    for t in range(N // 64):
+        cuts = sorted(set([0, K] + [32 * (u - t * KB) for u in b if t * KB < u < (t + 1) * KB]))
+        cols = slice(64 * t, 64 * t + 64)
+        np.testing.assert_array_equal(oracle.w8a8_acc_split(x, W[:, cols], cuts), ref[:, cols])
+
+
+def test_plan_shape_and_limits():
+    p = lib8.w8a8_plan(16, 4096, 1536)
+    assert p["n8_tiles"] == 2 and p["n_tiles"] == 24 and p["k_blocks"] == 128
+    assert p["blocks"] % 152 == 0 or p["blocks"] == p["slabs"]
+    assert p["smem_bytes"] * 2 <= 228 * 1024          # two CTAs per SM fit
+    for M in (1, 8, 9, 16, 17, 24, 25, 32):
+        assert lib8.w8a8_plan(M, 4096, 1536)["n8_tiles"] == (M + 7) // 8
+    # the size query covers every M up to M_max
+    big = lib8.w8a8_workspace_bytes(32, 4096, 1536)
+    assert all(lib8.w8a8_plan(M, 4096, 1536)["workspace_bytes"] <= big for M in range(1, 33))
+
+
+@pytest.mark.parametrize("M,K,N,blocks,code", [
+    (0, 512, 256, 0, 1), (33, 512, 256, 0, 1), (1, 0, 256, 0, 1), (1, 512, 0, 0, 1),
+    (1, 500, 256, 0, 2), (1, 512, 250, 0, 2), (1, 512, 256, -1, 1), (1, 512, 256, 10**6, 1)])
+def test_plan_rejects_bad_shapes(M, K, N, blocks, code):
+    p = lib8.PlanT()
+    assert lib8.lib().w8a8_plan(M, K, N, blocks, ctypes.byref(p)) == code
+    assert lib8.w8a8_workspace_bytes(M, K, N, blocks) == 0 or code == 0
+
+
+def test_calls_with_null_pointers_fail_before_any_launch():
+    L = lib8.lib()
+    null = ctypes.c_void_p(0)
+    assert L.w8a8_gemm(null, null, null, null, null, 1, 512, 256, 0, 0, null, 0, null) == 1
+    assert L.q8_0_gemv(null, null, null, null, 1, 512, 256, 0, null, 0, null) == 1
+    assert L.w8a8_pack_weights(null, 512, 256, null, null, 0, null) == 1
+    assert L.w8a8_workspace_init(null, 0, null) == 1
+
+
+def test_misaligned_and_short_workspace_are_rejected_on_the_host():
+    # Fake (never dereferenced) device addresses: the checks run before any launch.
+    L = lib8.lib()
+    a = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    ws_need = lib8.w8a8_workspace_bytes(16, 4096, 1536)
+    assert L.w8a8_gemm(odd, a, a, a, a, 16, 4096, 1536, 0, 0, a, ws_need, None) == 3
+    assert L.w8a8_gemm(a, a, odd, a, a, 16, 4096, 1536, 0, 0, a, ws_need, None) == 3
+    assert L.w8a8_gemm(a, a, a, a, a, 16, 4096, 1536, 0, 0, a, ws_need - 1, None) == 4
+    assert L.w8a8_gemm(a, a, a, a, a, 16, 4096, 1536, 0, 2, a, ws_need, None) == 1      # unknown flag
+    qws = lib8.q8_0_workspace_bytes(6, 4096, 320)
+    assert L.q8_0_gemv(odd, a, a, a, 6, 4096, 320, 0, a, qws, None) == 3
+    assert L.q8_0_gemv(a, a, a, a, 6, 4096, 320, 0, a, qws - 1, None) == 4
+    assert L.q8_0_gemv(a, a, a, a, 9, 4096, 320, 0, a, qws, None) == 1
+    assert L.q8_0_gemv(a, a, a, a, 6, 4016, 320, 0, a, qws, None) == 2      # K % 32 != 0
+
+
+# ------------------------------------------------------------------------------------------
+# CPU emulation of the GEMM kernel's fragment bookkeeping (documented layout + PTX fragments)
+# ------------------------------------------------------------------------------------------
+
+def _frag_a(words):
+    """mma.m16n8k16 A fragment of one lane from the kernel's conversion of 4 packed words.
+
+    Each word's bytes (0,2) form one register and bytes (1,3) another (as offset_bytes_to_half2).
+    Registers a0..a3 of one k16 step are (row g, slots 2c,2c+1), (row g+8, ...), (row g, slots
+    2c+8,2c+9), (row g+8, ...) per the PTX fragment layout; the kernel feeds
+    {lo(w_row_g), lo(w_row_g8), hi(w_row_g), hi(w_row_g8)}."""
+    def lohi(w):
+        b = [((w >> (8 * i)) & 0xFF) ^ 0x80 for i in range(4)]
+        b = [v - 256 if v >= 128 else v for v in b]
+        return (b[0], b[2]), (b[1], b[3])
+    return [lohi(w) for w in words]
+
+
+def test_emulated_fragment_path_reproduces_x_at_w():
+    M, K, N = 12, 64, 128
+    x, _, W, _ = synth.w8a8_inputs(M, K, N, seed=21)
+    packed = oracle.w8a8_pack(W)
+    KB = K // 32
+    NT8 = (M + 7) // 8
+    acc = np.zeros((N, 8 * NT8), dtype=np.int64)         # rows n, columns m (out^T)
+    xp = np.zeros((8 * NT8, K), dtype=np.int64)
+    xp[:M] = x
+    for t in range(N // 64):
+        for kb in range(KB):
+            for s in range(4):
+                base = (((t * KB + kb) * 4 + s) * 32) * 16
+                for lane in range(32):
+                    g, c = lane // 4, lane % 4
+                    wbytes = packed[base + lane * 16: base + lane * 16 + 16]
+                    words = [int.from_bytes(bytes(wbytes[4 * i:4 * i + 4]), "little") for i in range(4)]
+                    frag = _frag_a(words)
+                    for step in range(2):
+                        (r0l, r0h), (r1l, r1h) = frag[2 * step], frag[2 * step + 1]
+                        # slot -> k mapping used for both operands: slots (2c, 2c+1) <- k 8c+4step+{0,2};
+                        # slots (2c+8, 2c+9) <- k 8c+4step+{1,3}
+                        k0 = 32 * kb + 8 * c + 4 * step
+                        a_rows = {g: {2 * c: r0l[0], 2 * c + 1: r0l[1], 2 * c + 8: r0h[0], 2 * c + 9: r0h[1]},
+                                  g + 8: {2 * c: r1l[0], 2 * c + 1: r1l[1], 2 * c + 8: r1h[0], 2 * c + 9: r1h[1]}}
+                        slot_k = {2 * c: k0 + 0, 2 * c + 1: k0 + 2, 2 * c + 8: k0 + 1, 2 * c + 9: k0 + 3}
+                        for row, slots in a_rows.items():
+                            n = 64 * t + 16 * s + row
+                            for slot, a in slots.items():
+                                acc[n, :] += a * xp[:, slot_k[slot]]
+    ref = oracle.w8a8_acc(x, W)
+    np.testing.assert_array_equal(acc[:N, :M].T, ref)

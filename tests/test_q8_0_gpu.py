@@ -1,0 +1,121 @@
+"""Q8_0 weight GEMV on the GPU against the fp64 oracle.
+
+Tolerance, per output (t, n): |y_gpu - y64| <= 2e-3 * ||x_t||_2 * ||w_n||_2, with w_n the
+dequantised weight row.  This is the reading of the stated "2e-3, row-norm scaled, per output"
+bound: the Cauchy-Schwarz scale of the dot product.  It covers the fp32 summation and the final
+bf16 rounding (relative 2^-9 of |y| <= ||x_t|| ||w_n||).
+"""
+import numpy as np
+import pytest
+import torch
+
+import int8_weight_gemm_gb300 as lib8
+import oracle
+import synth
+from gpu_util import bf16_bits
+
+pytestmark = pytest.mark.gpu
+
+REL = 2e-3
+
+
+class Q8Case:
+    def __init__(self, T, K, N, seed, T_max=None):
+        self.x, self.q, self.d = synth.q8_0_inputs(T, K, N, seed=seed)
+        self.xd = self.x.cuda()
+        self.qd = torch.from_numpy(self.q).cuda()
+        self.dd = torch.from_numpy(self.d.view(np.int16)).cuda()
+        self.ws = lib8.alloc_workspace(lib8.q8_0_workspace_bytes(T_max or T, K, N))
+
+    def run(self, y=None, flags=0):
+        return lib8.q8_0_gemv(self.xd, self.qd, self.dd, self.ws, y=y, flags=flags)
+
+    def reference(self):
+        xb = self.x.view(torch.int16).numpy().view(np.uint16)
+        db = self.d.view(np.uint16)
+        return oracle.q8_0_gemv(xb, self.q, db), oracle.q8_0_bound(xb, self.q, db, REL)
+
+
+def _check(case):
+    y = case.run()
+    torch.cuda.synchronize()
+    got = y.float().cpu().numpy().astype(np.float64)
+    ref, bound = case.reference()
+    err = np.abs(got - ref)
+    worst = (err / bound).max()
+    assert (err <= bound).all(), f"max err/bound {worst:.3g}"
+    assert lib8.w8a8_workspace_status(case.ws) == 0
+    return got, ref
+
+
+@pytest.mark.parametrize("T", [1, 4, 6])
+@pytest.mark.parametrize("K,N", [(4096, 320), (320, 4096)])
+def test_verify_window_shapes(T, K, N):
+    _check(Q8Case(T, K, N, seed=100 * T + K))
+
+
+@pytest.mark.parametrize("T,K,N", [(8, 4096, 320), (2, 32, 16), (3, 64, 100), (5, 8192, 33), (7, 1024, 4096),
+                                   (1, 65536, 16), (6, 320, 1)])
+def test_edge_shapes(T, K, N):
+    _check(Q8Case(T, K, N, seed=T + K + N))
+
+
+def test_rows_beyond_t_untouched_and_replay_bitwise():
+    c = Q8Case(4, 4096, 320, seed=9, T_max=8)
+    y = torch.full((8, 320), 5.0, dtype=torch.bfloat16, device="cuda")
+    c.run(y=y[:4])
+    torch.cuda.synchronize()
+    assert (y[4:] == 5.0).all()
+    direct = bf16_bits(y[:4])
+    out = torch.empty((4, 320), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        c.run(y=out)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        c.run(y=out)
+    for _ in range(2):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(bf16_bits(out), direct)
+
+
+def test_the_quantised_bytes_are_read():
+    # Changing one quant (or one scale) moves exactly the outputs of its row, by the predicted
+    # amount: the kernel reads the Q8_0 bytes it is given.
+    c = Q8Case(3, 4096, 320, seed=4)
+    base, _ = _check(c)
+    c.q[17, 1000] = np.int8(-c.q[17, 1000] if c.q[17, 1000] != 0 else 9)
+    c.qd = torch.from_numpy(c.q).cuda()
+    got, _ = _check(c)
+    moved = np.nonzero((got != base).any(axis=0))[0]
+    assert set(moved.tolist()) == {17}
+    c.d[40, 3] = np.float16(c.d[40, 3] * 2)
+    c.dd = torch.from_numpy(c.d.view(np.int16)).cuda()
+    got2, _ = _check(c)
+    moved = np.nonzero((got2 != got).any(axis=0))[0]
+    assert set(moved.tolist()) == {40}
+
+
+def test_counters_reset_after_split_calls():
+    c = Q8Case(6, 4096, 320, seed=1)
+    for _ in range(3):
+        _check(c)
+    n_tiles = (320 + 15) // 16
+    ctr = c.ws[256:256 + 4 * n_tiles].view(torch.int32).cpu().numpy()
+    assert (ctr == 0).all()
+
+
+@pytest.mark.parametrize("K,N", [(4096, 320), (320, 4096)])
+def test_pdl_launch_matches_plain_launch_bitwise(K, N):
+    c = Q8Case(6, K, N, seed=77)
+    torch.cuda.synchronize()
+    plain = bf16_bits(c.run())
+    outs = [c.run(flags=lib8.W8A8_FLAG_PDL) for _ in range(4)]
+    torch.cuda.synchronize()
+    for o in outs:
+        np.testing.assert_array_equal(bf16_bits(o), plain)
+    _check(c)
