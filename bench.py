@@ -222,8 +222,11 @@ def time_gemm(M, K, N, dist, seed, steps, warmup, blocks=0, device=None, sample_
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
     per_call_us = sorted(s * 1e3 / C for s in step_ms)
+    plan = lib8.w8a8_plan(M, K, N, blocks)
     res = {
         "R": R, "C": C, "wbytes": wbytes, "total_ms": total_ms, "steps": steps,
+        "kernel": f"w8a8_gemm_kernel<{plan['n8_tiles']}, {plan['stages']}>",
+        "blocks": plan["blocks"],
         "us_median": statistics.median(per_call_us),
         "us_p90": per_call_us[min(len(per_call_us) - 1, int(0.9 * len(per_call_us)))],
         "avg_launch_us": total_ms * 1e3 / (steps * C),
@@ -359,7 +362,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} (copy, MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": traffic, "alg_bytes_per_launch": alg_bytes,
-                     "kernel": "w8a8_gemm_kernel<2,4,7>"},
+                     "kernel": res["kernel"]},
         "gpu_launches": res["launches"],
         "e2e": {k: (round(v, 3) if isinstance(v, float) else v) for k, v in res["e2e"].items()},
         "clocks": res["clocks"],
