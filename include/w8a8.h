@@ -163,6 +163,26 @@ int w8a8_plan(int M, int K, int N, int blocks, w8a8_plan_t* plan);
  * blocks + 1.  Host-only. */
 int w8a8_split_bounds(int K, int N, int blocks, long long* bounds, int n_bounds);
 
+/* W8A8 decode GEMM that allocates nothing and takes no workspace.  The pages have no counterpart:
+ * this entry point exists for callers that cannot provide device memory, such as a plugin that
+ * sees only the input and output pointers its host engine hands it, or a request path that must
+ * not call cudaMalloc (which can synchronise the device and stall other streams).
+ *
+ * Arguments, limits, result and errors are those of w8a8_gemm, without ws / ws_bytes.  The
+ * workspace is a 4 MiB area inside this library's device memory (a file-scope __device__ array,
+ * held on every device that loads the library until the process exits); a shape whose
+ * w8a8_workspace_bytes(M, K, N, blocks) exceeds 4 MiB returns W8A8_ERR_WORKSPACE_TOO_SMALL.
+ * Each call clears the part of the area it uses (one cudaMemsetAsync on `stream`) and then
+ * launches the kernel; it calls no allocating routine.
+ *
+ * The first call on a device looks up the area's device address (cudaGetSymbolAddress, with that
+ * device current) and caches it; make that first call before any stream capture on the device.
+ * All calls on a device share the one area, so calls whose kernels can overlap on the GPU (on
+ * different streams without ordering between them) race on it and give undefined results. */
+int w8a8_gemm_no_alloc(const int8_t* x_q, const float* x_scale, const void* W_packed,
+                       const float* w_scale, void* out, int M, int K, int N, int blocks,
+                       unsigned flags, void* stream);
+
 /* -------------------------------------------------------------------------------------------
  * Q8_0 weight GEMV (verify window)
  * ----------------------------------------------------------------------------------------- */

@@ -65,6 +65,7 @@ SIGNATURES = {
     "w8a8_workspace_bytes": ([_c_i, _c_i, _c_i, _c_i], _c_sz),
     "w8a8_pack_weights": ([_c_p, _c_i, _c_i, _c_p, _c_p, _c_sz, _c_p], _c_i),
     "w8a8_gemm": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_i, _c_i, _c_i, _c_i, ctypes.c_uint, _c_p, _c_sz, _c_p], _c_i),
+    "w8a8_gemm_no_alloc": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_i, _c_i, _c_i, _c_i, ctypes.c_uint, _c_p], _c_i),
     "w8a8_plan": ([_c_i, _c_i, _c_i, _c_i, ctypes.POINTER(PlanT)], _c_i),
     "w8a8_split_bounds": ([_c_i, _c_i, _c_i, ctypes.POINTER(ctypes.c_longlong), _c_i], _c_i),
     "q8_0_workspace_bytes": ([_c_i, _c_i, _c_i], _c_sz),

@@ -22,6 +22,10 @@ static int cuda_fail(cudaError_t e, const char* where) {
   return W8A8_ERR_CUDA;
 }
 
+int record_cuda_error(cudaError_t e, const char* where) { return cuda_fail(e, where); }
+
+void record_error(const char* text) { std::snprintf(g_last_error, sizeof(g_last_error), "%s", text); }
+
 static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Number of SMs of the current device; 152 (GB300) when no device can be queried, so that the

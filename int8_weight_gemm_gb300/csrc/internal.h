@@ -41,6 +41,10 @@ cudaError_t encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType type, voi
                                  const cuuint64_t* strides, const cuuint32_t* box, const cuuint32_t* estr,
                                  CUtensorMapSwizzle swizzle);
 
+// Record a CUDA error (returns W8A8_ERR_CUDA) or a plain message as this thread's last error text.
+int record_cuda_error(cudaError_t e, const char* where);
+void record_error(const char* text);
+
 // Raise a kernel's dynamic shared memory limit once per device.
 cudaError_t ensure_smem_attribute(const void* kernel, int bytes);
 
