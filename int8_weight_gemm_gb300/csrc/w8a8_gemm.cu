@@ -44,6 +44,10 @@ constexpr int kStageSlabs = 4;                     // one slab per consumer warp
 template <int NT8, int NS>
 struct GemmLayout {
   static_assert(kStageSlabs * kKBlock == 128, "the activation box row is one 128-byte swizzle span");
+  // Consumer warps split the stages by parity.  With an even ring depth every ring slot always holds
+  // stages of one parity, so each warp waits on every phase of its slots' barriers; with an odd
+  // depth a warp would skip phases and could not tell phase n from phase n + 2.
+  static_assert(NS % 2 == 0, "the ring depth must be even");
   static constexpr int kXRows = 8 * NT8;                    // activation rows loaded (zero past M)
   static constexpr int kXRawStage = kXRows * 128;           // raw int8 box, 128B-swizzled, 1 KiB multiple
   static constexpr int kWStage = kStageSlabs * kSlabBytes;
@@ -393,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
 // Host side
 // --------------------------------------------------------------------------------------------
 // Pipeline depth per n8-tile count, sized for two CTAs per SM.
-constexpr int kStages1 = 10, kStages2 = 9, kStages3 = 8, kStages4 = 7;
+constexpr int kStages1 = 10, kStages2 = 10, kStages3 = 8, kStages4 = 6;
 
 static int gemm_stages(int nt8) {
   switch (nt8) {

@@ -89,7 +89,10 @@ def test_plan_shape_and_limits():
     assert p["blocks"] % 152 == 0 or p["blocks"] == p["slabs"]
     assert p["smem_bytes"] * 2 <= 228 * 1024          # two CTAs per SM fit
     for M in (1, 8, 9, 16, 17, 24, 25, 32):
-        assert lib8.w8a8_plan(M, 4096, 1536)["n8_tiles"] == (M + 7) // 8
+        q = lib8.w8a8_plan(M, 4096, 1536)
+        assert q["n8_tiles"] == (M + 7) // 8
+        # consumer warps take stages by parity: an even ring keeps each slot with one parity group
+        assert q["stages"] % 2 == 0
     # the size query covers every M up to M_max
     big = lib8.w8a8_workspace_bytes(32, 4096, 1536)
     assert all(lib8.w8a8_plan(M, 4096, 1536)["workspace_bytes"] <= big for M in range(1, 33))
