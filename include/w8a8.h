@@ -100,7 +100,9 @@ int w8a8_workspace_status(void* ws, size_t ws_bytes, void* stream, uint32_t* sta
 size_t w8a8_packed_weight_bytes(int K, int N);
 
 /* Workspace bytes that w8a8_gemm needs for every M in [1, M_max] at this (K, N) and `blocks`
- * (0 = the automatic plan).  Returns 0 for arguments w8a8_gemm would reject. */
+ * (0 = the automatic plan, whose CTA count follows the current device's SM count).  Returns 0
+ * for arguments w8a8_gemm would reject.  Layout: a 256-byte header (status word first), then
+ * one 64-bit accumulator word per output element of every 64-row tile (zero between calls). */
 size_t w8a8_workspace_bytes(int M_max, int K, int N, int blocks);
 
 /* Pack W once, at load time and outside any timed region or capture (section 1.1 of the W8A8
@@ -169,9 +171,9 @@ int w8a8_split_bounds(int K, int N, int blocks, long long* bounds, int n_bounds)
  * not call cudaMalloc (which can synchronise the device and stall other streams).
  *
  * Arguments, limits, result and errors are those of w8a8_gemm, without ws / ws_bytes.  The
- * workspace is a 4 MiB area inside this library's device memory (a file-scope __device__ array,
+ * workspace is a 16 MiB area inside this library's device memory (a file-scope __device__ array,
  * held on every device that loads the library until the process exits); a shape whose
- * w8a8_workspace_bytes(M, K, N, blocks) exceeds 4 MiB returns W8A8_ERR_WORKSPACE_TOO_SMALL.
+ * w8a8_workspace_bytes(M, K, N, blocks) exceeds 16 MiB returns W8A8_ERR_WORKSPACE_TOO_SMALL.
  * Each call clears the part of the area it uses (one cudaMemsetAsync on `stream`) and then
  * launches the kernel; it calls no allocating routine.
  *

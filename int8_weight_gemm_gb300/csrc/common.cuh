@@ -176,6 +176,11 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// Bring the line holding *p into this SM's L1 (no register is written).
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 // Wait until the grids this one depends on have completed and their memory is visible.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -190,6 +195,14 @@ namespace w8a8 {
 // Fire-and-forget int32 add (no return value).
 __device__ __forceinline__ void red_add_s32(int* addr, int v) {
   asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
+// Returning 64-bit add with no ordering beyond the word itself (no compiler memory barrier
+// either: independent adds issue back to back).
+__device__ __forceinline__ unsigned long long atom_add_relaxed_u64(unsigned long long* addr, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.relaxed.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(addr), "l"(v));
+  return old;
 }
 
 // Counter arrival: releases this thread's earlier writes (and, through a preceding warp barrier,

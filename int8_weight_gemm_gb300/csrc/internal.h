@@ -15,7 +15,7 @@ struct GemmPlan {
   int nt8, n_tiles, kb;
   long long slabs;
   int blocks, threads, stage_slabs, stages;
-  size_t smem_bytes, workspace_bytes, counters_offset, partials_offset;
+  size_t smem_bytes, workspace_bytes, partials_offset;
 };
 
 int gemm_plan(int M, int K, int N, int blocks, int sm_count, GemmPlan* plan);

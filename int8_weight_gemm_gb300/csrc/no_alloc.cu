@@ -1,7 +1,6 @@
 // w8a8_gemm_no_alloc: the W8A8 decode GEMM for callers that cannot allocate device memory.
 //
-// w8a8_gemm needs a caller-provided workspace (split-tile arrival counters and int32 tile
-// accumulators).  Some callers have no way to provide one.  An inference plugin hosted inside
+// w8a8_gemm needs a caller-provided workspace (the split-tile accumulators).  Some callers have no way to provide one.  An inference plugin hosted inside
 // another engine sees only the input and output pointers the host engine hands it, with no access
 // to that engine's allocator.  A latency-critical request path may forbid cudaMalloc/cudaFree
 // outright, because those calls can synchronise the device and stall every other stream.  For
@@ -19,7 +18,7 @@
 namespace w8a8 {
 
 // Largest workspace this entry point can serve: a plan needing more is rejected.
-constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 
 // The scratch area.  In host code this name is only a stand-in for the device symbol: its device
 // address must be obtained with cudaGetSymbolAddress on each device (see scratch_on_current_device).
@@ -67,7 +66,7 @@ extern "C" int w8a8_gemm_no_alloc(const int8_t* x_q, const float* x_scale, const
       misaligned(w_scale, 4))
     return W8A8_ERR_MISALIGNED;
   if (pl.workspace_bytes > kNoAllocScratchBytes) {
-    record_error("w8a8_gemm_no_alloc: this shape needs more scratch than the built-in 4 MiB area");
+    record_error("w8a8_gemm_no_alloc: this shape needs more scratch than the built-in 16 MiB area");
     return W8A8_ERR_WORKSPACE_TOO_SMALL;
   }
   void* ws = nullptr;
@@ -75,7 +74,7 @@ extern "C" int w8a8_gemm_no_alloc(const int8_t* x_q, const float* x_scale, const
   if (e != cudaSuccess) return record_cuda_error(e, "w8a8_gemm_no_alloc (scratch address)");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The area keeps whatever the previous call left there: clear the part this call relies on
-  // (status word, arrival counters, split-tile accumulators) before the kernel reads it.
+  // (status word and split-tile accumulators) before the kernel reads it.
   e = cudaMemsetAsync(ws, 0, pl.workspace_bytes, s);
   if (e != cudaSuccess) return record_cuda_error(e, "w8a8_gemm_no_alloc (scratch clear)");
   e = gemm_launch(pl, x_q, x_scale, W_packed, w_scale, out, M, K, N, ws, (flags & W8A8_FLAG_PDL) != 0, s);

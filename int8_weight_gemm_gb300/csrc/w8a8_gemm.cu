@@ -6,8 +6,10 @@
 //    kernel streams it as one contiguous byte range per CTA;
 //  * split-K over a CTA count tied to the SM count (first rule), generalised to equal runs of
 //    2 KiB slabs over the linearised (tile, k-block) space, all cuts on 32-aligned k;
-//  * a fused last-arrival combine (qkv recipe: counter per output tile, fence + atomic, the last
-//    arriver sums the partials in ascending order, scales and stores bf16) in one launch;
+//  * a fused last-arrival combine in one launch (qkv recipe: the last arriver at a split tile
+//    holds the complete sum, scales it and stores bf16).  The recipe's per-tile counter, fence
+//    and read-back become one returning 64-bit atomic per output element that carries both the
+//    arrival count and the biased int32 sum, spread over all consumer threads;
 //  * exact int32 sums, k-ascending within a split and ascending over splits.
 //
 // GB300 choices (prior art on the pages is gfx928 DUMMA; none of it carries over literally):
@@ -36,7 +38,7 @@ constexpr int kSlabBytes = kTileRows * kKBlock;    // 2048
 constexpr int kConsumerWarps = 8;                  // two per stage slot: even / odd stages
 constexpr int kWarpsPerStage = 4;                  // one slab of a stage each
 constexpr int kSubTiles = 4;                       // 16-row sub-tiles of a 64-row tile
-constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kThreads = 32 * (kConsumerWarps + 1);   // + one producer warp
 constexpr int kFlushSlabs = 16;                    // 16 slabs of 32 k = 512 k per warp between int32 flushes
 
 constexpr int kStageSlabs = 4;                     // one slab per consumer warp per stage
@@ -51,7 +53,7 @@ struct GemmLayout {
   static constexpr int kXRows = 8 * NT8;                    // activation rows loaded (zero past M)
   static constexpr int kXRawStage = kXRows * 128;           // raw int8 box, 128B-swizzled, 1 KiB multiple
   static constexpr int kWStage = kStageSlabs * kSlabBytes;
-  static constexpr int kSegSumInts = 2 * 4 * NT8 * 32 * 4;  // two int32 [sub][j][lane][4] segment sums
+  static constexpr int kSegSumInts = 2 * 4 * NT8 * 4 * 32;  // two int32 [sub][j][r][lane] segment sums
   static constexpr int kBytes = 1024 + NS * (kXRawStage + kWStage) + kSegSumInts * 4;   // + alignment slack
 };
 
@@ -96,8 +98,10 @@ struct GemmParams {
   const float* w_scale;
   uint16_t* out;
   uint32_t* status;
-  uint32_t* counters;
-  int4* tile_acc;     // per 16-row sub-tile: int32 accumulator of split tiles, zero between calls
+  // One 64-bit word per output element of every tile: (arrivals << 52) + sum of (partial + 2^31)
+  // over the CTAs that have added their partial so far; zero between calls.  Layout
+  // [tile][sub-tile][n8 tile][fragment register][lane].
+  unsigned long long* tile_acc;
   int M, K, N, KB;
   long long U;
   int G;
@@ -105,64 +109,71 @@ struct GemmParams {
 };
 
 // Walks a CTA's run of slabs [b0, b1) as stages of at most SS slabs that never cross a tile.
+// Slab indices fit in 32 bits (at most 2^14 tiles x 2^11 k-blocks).
 struct StageIter {
-  long long u, b1, seg_begin, seg_end, t;
+  int u, b1, seg_begin, seg_end, t;
   int KB, ns, ss;
-  __device__ StageIter(long long b0_, long long b1_, int KB_, int ss_) : u(b0_), b1(b1_), KB(KB_), ss(ss_) {
-    begin_segment();
-  }
+  __device__ StageIter(int b0_, int b1_, int KB_, int ss_) : u(b0_), b1(b1_), KB(KB_), ss(ss_) { begin_segment(); }
   __device__ void begin_segment() {
     t = u / KB;
     seg_begin = u;
-    seg_end = min(b1, (t + 1) * (long long)KB);
-    ns = (int)min((long long)ss, seg_end - u);
+    seg_end = min(b1, (t + 1) * KB);
+    ns = min(ss, seg_end - u);
   }
   __device__ bool done() const { return u >= b1; }
-  __device__ int kb0() const { return (int)(u - t * KB); }
+  __device__ int kb0() const { return u - t * KB; }
   __device__ bool last_of_segment() const { return u + ns >= seg_end; }
   __device__ void next() {
     u += ns;
     if (u >= b1) return;
     if (u >= seg_end) begin_segment();
-    else ns = (int)min((long long)ss, seg_end - u);
+    else ns = min(ss, seg_end - u);
   }
 };
 
-// out[m][n] for this lane's accumulator fragment: (row g / g+8 of the sub-tile) x (columns
-// 2c, 2c+1 of each n8 tile).  xs holds x_scale of the lane's columns, wsc w_scale of its rows.
+// Index of a fragment value in a segment sum (shared) or a tile accumulator (global): lanes are
+// innermost, so a warp's 32 accesses of one (sub-tile, n8 tile, register) are contiguous.
 template <int NT8>
-__device__ __forceinline__ void store_epilogue(const GemmParams& p, const int (&v)[NT8][4], const float (&xs)[NT8][2],
-                                               const float (&wsc)[2], int n0, int g, int c) {
-#pragma unroll
-  for (int j = 0; j < NT8; ++j) {
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int m = 8 * j + 2 * c + (r & 1);
-      const int n = n0 + g + 8 * (r >> 1);
-      if (m < p.M && n < p.N) {
-        float f = __int2float_rn(v[j][r]);
-        f = __fmul_rn(f, xs[j][r & 1]);
-        f = __fmul_rn(f, wsc[r >> 1]);
-        p.out[(long long)m * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(f));
-      }
-    }
+__device__ __forceinline__ int frag_index(int u, int j, int r, int lane) {
+  return ((u * NT8 + j) * 4 + r) * 32 + lane;
+}
+
+// Epilogue of one output element: out[m][n] = bf16_rne((float(acc) * x_scale[m]) * w_scale[n]).
+__device__ __forceinline__ void store_out(const GemmParams& p, int m, int n, int acc, float xsv, float wsv) {
+  if (m < p.M && n < p.N) {
+    float f = __int2float_rn(acc);
+    f = __fmul_rn(f, xsv);
+    f = __fmul_rn(f, wsv);
+    p.out[(long long)m * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(f));
   }
 }
+
+constexpr int kProducerWarp = kConsumerWarps;        // warp 8: lane 0 issues every copy
+constexpr int kConsumerThreads = 32 * kConsumerWarps;
+constexpr int kSegmentBarrier = 1;                   // named barrier of the consumer warps
 
 template <int NT8, int NS>
 __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_constant__ GemmParams p) {
   using L = GemmLayout<NT8, NS>;
+  constexpr int kSegInts = L::kSegSumInts / 2;      // one segment-sum buffer
+  constexpr int kPer = kSegInts / kConsumerThreads; // output elements per consumer thread at a segment end
+  static_assert(kPer * kConsumerThreads == kSegInts, "segment sums split evenly over the consumers");
+  // Work split of the consumer warps.  NT8 <= 2: warp w takes slab w % 4 of the stages of parity
+  // w / 4, all four sub-tiles.  NT8 >= 3 (the accumulators of four sub-tiles would not fit the
+  // register budget): warp w takes slab w % 4 of every stage, sub-tiles 2 (w / 4) and 2 (w / 4) + 1.
+  constexpr bool kHalfSubTiles = NT8 >= 3;
+  constexpr int kWarpSubTiles = kHalfSubTiles ? kSubTiles / 2 : kSubTiles;
+  constexpr int kStageWarps = kHalfSubTiles ? kConsumerWarps : kWarpsPerStage;   // consumers of a stage
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[NS];   // W slabs + raw activation box of a stage landed
   __shared__ __align__(8) uint64_t empty_bar[NS];  // the stage's consumer warps took their slabs
-  __shared__ __align__(8) uint64_t seg_bar;        // all consumer threads added a segment's sums
   __shared__ int abort_flag;
 
   // 128B-swizzled TMA boxes need a 1 KiB aligned destination.
   uint8_t* const smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* const xraw = smem;
   uint8_t* const wring = xraw + NS * L::kXRawStage;
-  int* const segsum = reinterpret_cast<int*>(wring + NS * L::kWStage);   // [2][sub][j][lane][4] int32
+  int* const segsum = reinterpret_cast<int*>(wring + NS * L::kWStage);   // [2][sub][j][r][lane] int32
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -170,9 +181,8 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
 #pragma unroll
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], kWarpsPerStage);
+      mbar_init(&empty_bar[s], kStageWarps);
     }
-    mbar_init(&seg_bar, 32 * kConsumerWarps);
     abort_flag = 0;
     mbar_fence_init();
   }
@@ -180,10 +190,10 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
   __syncthreads();
   pdl_trigger();   // the next call on the stream may start its own weight prefetch
 
-  const long long b0 = split_lo(blockIdx.x, p.U, p.G);
-  const long long b1 = split_lo(blockIdx.x + 1, p.U, p.G);
+  const int b0 = (int)split_lo(blockIdx.x, p.U, p.G);
+  const int b1 = (int)split_lo(blockIdx.x + 1, p.U, p.G);
 
-  if (warp == kConsumerWarps) {
+  if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- producer (one thread)
     if (lane != 0) return;
     tma_prefetch_desc(&p.xmap);
@@ -198,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
       int npre = 0;
       while (npre < NS && !pre.done()) {
         mbar_arrive_expect_tx(&full_bar[npre], (uint32_t)(pre.ns * kSlabBytes) + xbox);
-        bulk_g2s_hint(wring + npre * L::kWStage, p.wp + pre.u * kSlabBytes, (uint32_t)(pre.ns * kSlabBytes),
+        bulk_g2s_hint(wring + npre * L::kWStage, p.wp + (size_t)pre.u * kSlabBytes, (uint32_t)(pre.ns * kSlabBytes),
                       &full_bar[npre], policy);
         pre.next();
         ++npre;
@@ -213,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
       const int s = q % NS;
       if (q >= NS && !mbar_wait(&empty_bar[s], ((q / NS) & 1) ^ 1, &abort_flag, p.status)) break;
       mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(it.ns * kSlabBytes) + xbox);
-      bulk_g2s_hint(wring + s * L::kWStage, p.wp + it.u * kSlabBytes, (uint32_t)(it.ns * kSlabBytes), &full_bar[s],
+      bulk_g2s_hint(wring + s * L::kWStage, p.wp + (size_t)it.u * kSlabBytes, (uint32_t)(it.ns * kSlabBytes), &full_bar[s],
                     policy);
       tma_load_2d(xraw + s * L::kXRawStage, &p.xmap, it.kb0() * kKBlock, 0, &full_bar[s]);
     }
@@ -229,62 +239,54 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
   // Warp w multiplies slab (w % 4) of every stage of parity (w / 4), covering all four 16-row
   // sub-tiles of the 64-row tile.  Each warp converts only its own 32-k activation slice, so the
   // warps never wait for one another inside a tile.  Their fp32 partials (exact integers) are
-  // flushed as int32 into a shared per-segment sum; warps 0..3 finish sub-tiles 0..3.
-  pdl_wait();
+  // flushed as int32 into the segment's shared sum buffer (two buffers, used by alternate
+  // segments).  At the end of each segment all consumer threads finish it together: every thread
+  // takes kPer of its output elements (one returning atomic each for a split tile), so the tail
+  // of a segment is one global round trip.  Meanwhile the producer keeps filling the ring.
+  pdl_wait();   // x_scale, w_scale, out and the accumulators may belong to the previous call
   const int g = lane >> 2, c = lane & 3;
   const int slab = warp & (kStageSlabs - 1);
-  const int parity = warp / kStageSlabs;
-  float xs[NT8][2];
-  float wsc[2] = {0.f, 0.f};
+  const int half = warp / kStageSlabs;
+  const int sub0 = kHalfSubTiles ? kWarpSubTiles * half : 0;   // first sub-tile of this warp
+  float facc[kWarpSubTiles][NT8][4];
 #pragma unroll
-  for (int j = 0; j < NT8; ++j)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int m = 8 * j + 2 * c + e;
-      xs[j][e] = (warp < 4 && m < p.M) ? __ldg(p.x_scale + m) : 0.f;
-    }
-  float facc[4][NT8][4];
-#pragma unroll
-  for (int u = 0; u < 4; ++u)
+  for (int u = 0; u < kWarpSubTiles; ++u)
 #pragma unroll
     for (int j = 0; j < NT8; ++j)
 #pragma unroll
       for (int r = 0; r < 4; ++r) facc[u][j][r] = 0.f;
-  int since = 0;   // slabs accumulated in fp32 by this warp since its last flush
+  int since = 0;          // slabs accumulated in fp32 by this warp since its last flush
   int segs = 0;
   int q = 0;
-
+  uint32_t arrivals = 0;  // CTAs whose runs share the current segment's tile
   // Add this warp's fp32 partial sums (exact integers) into the segment's shared int32 sums.
   auto flush = [&](int* dst) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < kWarpSubTiles; ++u)
 #pragma unroll
       for (int j = 0; j < NT8; ++j)
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          const int v = __float2int_rn(facc[u][j][r]);
-          if (v != 0) atomicAdd(dst + ((u * NT8 + j) * 32 + lane) * 4 + r, v);
+          atomicAdd(dst + frag_index<NT8>(sub0 + u, j, r, lane), __float2int_rn(facc[u][j][r]));
           facc[u][j][r] = 0.f;
         }
   };
 
   for (StageIter it(b0, b1, p.KB, kStageSlabs); !it.done(); it.next(), ++q) {
     const int s = q % NS;
-    if (it.u == it.seg_begin && warp < 4) {
-      // Start of a tile segment: fetch the w_scale values this warp's epilogue will need now, so
-      // that their latency hides behind the segment's stream.
-      const int nr = (int)(it.t * kTileRows) + 16 * warp + g;
-      wsc[0] = nr < p.N ? __ldg(p.w_scale + nr) : 0.f;
-      wsc[1] = nr + 8 < p.N ? __ldg(p.w_scale + nr + 8) : 0.f;
+    if (it.u == it.seg_begin) {
+      // Start of a segment: count the tile's contributors now, off the segment's tail.
+      const long long t = it.t;
+      arrivals = (uint32_t)(split_owner((t + 1) * p.KB - 1, p.U, p.G) - split_owner(t * p.KB, p.U, p.G) + 1);
     }
-    if ((q & 1) == parity) {
+    if (kHalfSubTiles || (q & 1) == half) {
       if (!mbar_wait(&full_bar[s], (uint32_t)((q / NS) & 1), &abort_flag, p.status)) return;
       if (slab < it.ns) {
-        // Weight fragments of the four sub-tiles, then this slab's activation B fragments.
-        const uint8_t* wst = wring + s * L::kWStage + slab * kSlabBytes + lane * 16;
-        uint4 w[4];
+        // Weight fragments of this warp's sub-tiles, then this slab's activation B fragments.
+        const uint8_t* wst = wring + s * L::kWStage + slab * kSlabBytes + sub0 * 512 + lane * 16;
+        uint4 w[kWarpSubTiles];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) w[u] = *reinterpret_cast<const uint4*>(wst + u * 512);
+        for (int u = 0; u < kWarpSubTiles; ++u) w[u] = *reinterpret_cast<const uint4*>(wst + u * 512);
         // Row m of the box sits at m * 128 with its 16-byte chunks XOR-swizzled by (m & 7) = g.
         const uint8_t* xr = xraw + s * L::kXRawStage;
         const int chunk = 2 * slab + (c >> 1);
@@ -298,11 +300,11 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);   // registers hold everything this warp needs
         if (since == kFlushSlabs) {
-          flush(segsum + (segs & 1) * L::kSegSumInts / 2);
+          flush(segsum + (segs & 1) * kSegInts);
           since = 0;
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kWarpSubTiles; ++u) {
           uint32_t a[2][4];
           offset_bytes_to_half2(w[u].x, a[0][0], a[0][2]);   // row g,   k 8c+0..3
           offset_bytes_to_half2(w[u].y, a[0][1], a[0][3]);   // row g+8, k 8c+0..3
@@ -323,73 +325,72 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
     if (!it.last_of_segment()) continue;
 
     // ------------------------------------------------------------ end of this CTA's part of a tile
-    int* const sums = segsum + (segs & 1) * L::kSegSumInts / 2;
+    // Element e = threadIdx.x + kConsumerThreads * i of the segment sums (layout [sub][j][r][lane])
+    // is this thread's i-th output element.  Its scales are prefetched into L1 first, so that
+    // their latency hides behind the flush and the barrier.
+    const int n_tile = it.t * kTileRows;
+    // Row m and column n of element e: the inverse of frag_index and of the accumulator fragment
+    // (lane = 4g + c holds rows 2c + (r & 1) of n8 tile j and columns g + 8 (r >> 1) of sub-tile u).
+    auto elem_m = [&](int i) {
+      const int e = threadIdx.x + kConsumerThreads * i;
+      return 8 * ((e >> 7) % NT8) + 2 * (e & 3) + ((e >> 5) & 1);
+    };
+    auto elem_n = [&](int i) {
+      const int e = threadIdx.x + kConsumerThreads * i;
+      return n_tile + 16 * ((e >> 7) / NT8) + ((e & 31) >> 2) + 8 * ((e >> 6) & 1);
+    };
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int m = elem_m(i), n = elem_n(i);
+      if (m < p.M) prefetch_l1(p.x_scale + m);
+      if (n < p.N) prefetch_l1(p.w_scale + n);
+    }
+    int* const sums = segsum + (segs & 1) * kSegInts;
     if (since) flush(sums);
     since = 0;
-    mbar_arrive(&seg_bar);
-    if (!mbar_wait(&seg_bar, (uint32_t)(segs & 1), &abort_flag, p.status)) return;
     ++segs;
-    if (warp >= 4) continue;
-    // Warp `sub` takes sub-tile `sub` of the segment's sums and clears them for segment segs + 1
-    // (the next user of this buffer waits on a later segment barrier, which these warps reach
-    // only after the clear).
-    const int sub = warp;
-    int part[NT8][4];
-#pragma unroll
-    for (int j = 0; j < NT8; ++j) {
-      int4* cell = reinterpret_cast<int4*>(sums) + (sub * NT8 + j) * 32 + lane;
-      const int4 v = *cell;
-      part[j][0] = v.x;
-      part[j][1] = v.y;
-      part[j][2] = v.z;
-      part[j][3] = v.w;
-      *cell = make_int4(0, 0, 0, 0);
-    }
-    const long long t = it.t;
-    const int n0 = (int)(t * kTileRows) + 16 * sub;
+    // Every consumer's part is in the sums.  The buffer is next written two segments later, after
+    // the next segment's barrier, which each thread reaches only after its reads and clears here.
+    named_bar_sync(kSegmentBarrier, kConsumerThreads);
+    const int t = it.t;
+    int* const mine = sums + threadIdx.x;   // element i at mine[kConsumerThreads * i]
+    auto finish = [&](int i, int total) {    // scales were prefetched into L1 above
+      const int m = elem_m(i), n = elem_n(i);
+      store_out(p, m, n, total, m < p.M ? __ldg(p.x_scale + m) : 0.f, n < p.N ? __ldg(p.w_scale + n) : 0.f);
+    };
     if (it.seg_begin == t * p.KB && it.seg_end == (t + 1) * p.KB) {   // the whole tile is ours
-      store_epilogue<NT8>(p, part, xs, wsc, n0, g, c);
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        finish(i, mine[kConsumerThreads * i]);
+        mine[kConsumerThreads * i] = 0;
+      }
       continue;
     }
-    // Split tile (qkv recipe's fused tail): add the int32 partial into the tile's accumulator in
-    // the workspace, make it visible GPU-wide, then count the arrival.  int32 addition is
-    // associative, so the total is the same bits as an ascending-order sum of the partials.  The
-    // last arrival reads the total (its own partial included), returns the accumulator and the
-    // counter to zero for the next call, and stores the bf16 tile.
-    int* tacc = reinterpret_cast<int*>(p.tile_acc + (t * kSubTiles + sub) * (NT8 * 32)) + lane * 4;
+    // Split tile.  Each element's word counts its arrivals in bits 52..63 and sums the partials,
+    // each offset by 2^31 so that it is a non-negative 32-bit number, in bits 0..51 (at most 2048
+    // CTAs share a tile, so neither field overflows).  int32 addition is associative, so the CTA
+    // that brings the count to n holds the same total, in the same bits, as an ascending-order
+    // sum of the n partials; it stores the bf16 result and returns the word to zero for the next
+    // call.  One returning atomic per element: no separate counter, fence or read-back.
+    const uint32_t n = arrivals;
+    unsigned long long* const tacc = p.tile_acc + (size_t)t * kSegInts + threadIdx.x;
+    unsigned long long old[kPer];
 #pragma unroll
-    for (int j = 0; j < NT8; ++j)
+    for (int i = 0; i < kPer; ++i)
+      old[i] = atom_add_relaxed_u64(tacc + kConsumerThreads * i,
+                                    (1ull << 52) + ((uint32_t)mine[kConsumerThreads * i] ^ 0x80000000u));
 #pragma unroll
-      for (int r = 0; r < 4; ++r) red_add_s32(tacc + j * 128 + r, part[j][r]);
-    __threadfence();
-    __syncwarp();
-    const long long i_lo = split_owner(t * p.KB, p.U, p.G);
-    const long long i_hi = split_owner((t + 1) * p.KB - 1, p.U, p.G);
-    const uint32_t arrivals = (uint32_t)(i_hi - i_lo + 1);
-    uint32_t* ctr = p.counters + t * kSubTiles + sub;
-    uint32_t old = 0;
-    if (lane == 0) old = atom_add_acq_rel_u32(ctr, 1u);
-    old = __shfl_sync(0xffffffffu, old, 0);
-    if (old >= arrivals) {
-      if (lane == 0) atomicOr(p.status, W8A8_DEV_COUNTER_CORRUPT);
-      continue;
+    for (int i = 0; i < kPer; ++i) {
+      const uint32_t arrived = (uint32_t)(old[i] >> 52);
+      const uint32_t biased = (uint32_t)mine[kConsumerThreads * i] ^ 0x80000000u;
+      mine[kConsumerThreads * i] = 0;
+      if (arrived == n - 1) {
+        tacc[kConsumerThreads * i] = 0ull;
+        finish(i, (int)((uint32_t)old[i] + biased - ((n & 1u) << 31)));   // biased sum - n * 2^31, mod 2^32
+      } else if (arrived >= n) {
+        atomicOr(p.status, W8A8_DEV_COUNTER_CORRUPT);
+      }
     }
-    if (old != arrivals - 1) continue;
-    __syncwarp();
-    __threadfence();
-    int tot[NT8][4];
-#pragma unroll
-    for (int j = 0; j < NT8; ++j) {
-      const int4 v = __ldcg(reinterpret_cast<const int4*>(tacc + j * 128));
-      tot[j][0] = v.x;
-      tot[j][1] = v.y;
-      tot[j][2] = v.z;
-      tot[j][3] = v.w;
-    }
-#pragma unroll
-    for (int j = 0; j < NT8; ++j) __stcg(reinterpret_cast<int4*>(tacc + j * 128), make_int4(0, 0, 0, 0));
-    if (lane == 0) *reinterpret_cast<volatile uint32_t*>(ctr) = 0u;
-    store_epilogue<NT8>(p, tot, xs, wsc, n0, g, c);
   }
 }
 
@@ -417,7 +418,36 @@ static size_t gemm_smem_bytes(int nt8) {
   }
 }
 
-static constexpr int kAutoCtasPerSm = 2;
+static constexpr int kAutoCtasPerSm = 2;   // resident CTAs per SM (shared memory and registers)
+
+// Automatic CTA count.  More CTAs stream the weight faster, but every split tile adds one partial
+// per CTA that shares it, and the partials meet in the L2 atomic units at the end of the call
+// (measured: about 22.5 ps per partial value when all CTAs finish together).  Measured stream
+// rates: a CTA alone on its SM about 25 GB/s; two CTAs on every SM about 20 GB/s each, and the
+// whole part about 6 TB/s.  CTA counts between one and two per SM leave the SMs that hold two
+// CTAs as the slowest, so the candidates are up to one CTA per SM (multiples of an eighth of the
+// SM count) and exactly two per SM; the plan takes the lowest modelled time.
+static int auto_blocks(long long slabs, int n_tiles, int nt8, int sm_count) {
+  const double weight_bytes = (double)slabs * kSlabBytes;
+  const double sec_per_partial = 22.5e-12;
+  const int sms = sm_count > 0 ? sm_count : 152;
+  int best = 0;
+  double best_t = 0.0;
+  for (int k = 4; k <= 9; ++k) {
+    const long long g = k <= 8 ? (long long)k * sms / 8 : (long long)kAutoCtasPerSm * sms;
+    if (g < 1 || g > slabs) continue;
+    double rate = k <= 8 ? (double)g * 25e9 : (double)g * 20e9;
+    if (rate > 6.0e12) rate = 6.0e12;
+    // Split segments that finish together at the end: with at least as many CTAs as tiles every
+    // tile is cut (about g + n_tiles segments, all ending with the runs); with fewer, each CTA's
+    // last segment (the first one ends early and its partial overlaps the stream).
+    const double split_segments = (double)(g >= n_tiles ? g + n_tiles : g);
+    const double t = weight_bytes / rate + sec_per_partial * 512.0 * nt8 * split_segments;
+    if (best == 0 || t < best_t) best = (int)g, best_t = t;
+  }
+  if (best == 0) best = (int)(slabs < (long long)kAutoCtasPerSm * sms ? slabs : (long long)kAutoCtasPerSm * sms);
+  return best;
+}
 
 int gemm_plan(int M, int K, int N, int blocks, int sm_count, GemmPlan* plan) {
   if (M < 1 || M > 32 || K < 1 || K > 65536 || N < 1 || N > 1048576 || blocks < 0) return W8A8_ERR_INVALID_ARG;
@@ -428,8 +458,7 @@ int gemm_plan(int M, int K, int N, int blocks, int sm_count, GemmPlan* plan) {
   pl.kb = K / kKBlock;
   pl.slabs = (long long)pl.n_tiles * pl.kb;
   if (blocks == 0) {
-    long long g = (long long)kAutoCtasPerSm * (sm_count > 0 ? sm_count : 152);
-    pl.blocks = (int)(g < pl.slabs ? g : pl.slabs);
+    pl.blocks = auto_blocks(pl.slabs, pl.n_tiles, pl.nt8, sm_count);
   } else {
     if (blocks > pl.slabs) return W8A8_ERR_INVALID_ARG;
     pl.blocks = blocks;
@@ -438,11 +467,10 @@ int gemm_plan(int M, int K, int N, int blocks, int sm_count, GemmPlan* plan) {
   pl.stage_slabs = kStageSlabs;
   pl.stages = gemm_stages(pl.nt8);
   pl.smem_bytes = gemm_smem_bytes(pl.nt8);
-  const size_t counters = ((size_t)pl.n_tiles * kSubTiles * 4 + 255) / 256 * 256;
-  const size_t partials = (size_t)pl.n_tiles * kSubTiles * pl.nt8 * 32 * 16;   // tile accumulators
-  pl.counters_offset = kWsHeaderBytes;
-  pl.partials_offset = kWsHeaderBytes + counters;
-  pl.workspace_bytes = kWsHeaderBytes + counters + partials;
+  // One 64-bit (arrival count, biased sum) word per output element of every tile.
+  const size_t partials = (size_t)pl.n_tiles * kSubTiles * pl.nt8 * 4 * 32 * sizeof(unsigned long long);
+  pl.partials_offset = kWsHeaderBytes;
+  pl.workspace_bytes = kWsHeaderBytes + partials;
   *plan = pl;
   return W8A8_OK;
 }
@@ -484,8 +512,7 @@ cudaError_t gemm_launch(const GemmPlan& pl, const int8_t* x, const float* xs, co
   p.w_scale = wsc;
   p.out = static_cast<uint16_t*>(out);
   p.status = static_cast<uint32_t*>(ws);
-  p.counters = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + pl.counters_offset);
-  p.tile_acc = reinterpret_cast<int4*>(static_cast<uint8_t*>(ws) + pl.partials_offset);
+  p.tile_acc = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(ws) + pl.partials_offset);
   p.M = M;
   p.K = K;
   p.N = N;

@@ -143,8 +143,8 @@ def test_counters_return_to_zero_and_calls_repeat():
     for blocks in (0, 1, 304, 3072, 5, 0):
         got = bf16_bits(case.run(blocks=blocks))
         np.testing.assert_array_equal(got, ref)
-    # Between calls the whole workspace past its status word is zero again: arrival counters and
-    # split-tile accumulators are returned to zero by each tile's last arrival.
+    # Between calls the whole workspace past its status word is zero again: each split-tile
+    # accumulator word is returned to zero by the element's last arrival.
     torch.cuda.synchronize()
     assert (case.ws[4:] == 0).all()
     assert case.status() == 0

@@ -45,15 +45,16 @@ def test_no_alloc_matches_workspace_entry_point_twice(M, K, N, blocks):
 
 
 def test_no_alloc_rejects_shapes_beyond_its_scratch():
-    # M = 32 at N = 32768 + 64 needs 513 tiles x 8 KiB of accumulators: more than the 4 MiB area.
-    M, K, N = 32, 32, 32832
+    # M = 32 at N = 131072 + 64 has 2049 tiles of 16 KiB of split-tile accumulators: more than the
+    # 16 MiB area.
+    M, K, N = 32, 32, 131136
     x = torch.zeros((M, K), dtype=torch.int8, device="cuda")
     xs = torch.ones(M, dtype=torch.float32, device="cuda")
     wp = torch.zeros(lib8.w8a8_packed_weight_bytes(K, N), dtype=torch.uint8, device="cuda")
     wsc = torch.ones(N, dtype=torch.float32, device="cuda")
     out = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
-    assert lib8.w8a8_workspace_bytes(M, K, N) > (4 << 20)
+    assert lib8.w8a8_workspace_bytes(M, K, N) > (16 << 20)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     rc = lib8.lib().w8a8_gemm_no_alloc(_ptr(x), _ptr(xs), _ptr(wp), _ptr(wsc), _ptr(out), M, K, N, 0, 0, stream)
     assert rc == 4
-    assert b"4 MiB" in lib8.lib().w8a8_last_error()
+    assert b"16 MiB" in lib8.lib().w8a8_last_error()
