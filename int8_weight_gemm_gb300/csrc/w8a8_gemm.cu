@@ -167,6 +167,8 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[NS];   // W slabs + raw activation box of a stage landed
   __shared__ __align__(8) uint64_t empty_bar[NS];  // the stage's consumer warps took their slabs
+  __shared__ float xs_sm[32];                      // x_scale (0 past M)
+  __shared__ float ws_sm[2][kTileRows];            // w_scale of a segment's tile, by segment parity
   __shared__ int abort_flag;
 
   // 128B-swizzled TMA boxes need a 1 KiB aligned destination.
@@ -259,6 +261,12 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
   int segs = 0;
   int q = 0;
   uint32_t arrivals = 0;  // CTAs whose runs share the current segment's tile
+  // Scales are fetched into registers long before they are needed (x_scale at the start, a
+  // tile's w_scale at the start of its segment) and parked in shared memory just before the
+  // segment barrier: loads issued at the very end of the call, when every CTA issues them at
+  // once, were measured to stall the epilogue for microseconds.
+  const float xs_reg = threadIdx.x < 32 && (int)threadIdx.x < p.M ? __ldg(p.x_scale + threadIdx.x) : 0.f;
+  float ws_reg = 0.f;
   // Add this warp's fp32 partial sums (exact integers) into the segment's shared int32 sums.
   auto flush = [&](int* dst) {
 #pragma unroll
@@ -272,12 +280,48 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
         }
   };
 
+  // Output element i of this thread at a segment end: element e = threadIdx.x + kConsumerThreads * i
+  // of the segment sums (layout [sub][j][r][lane]).  Its row m and column n are the inverse of
+  // frag_index and of the accumulator fragment (lane = 4g + c holds rows 2c + (r & 1) of n8 tile j
+  // and columns g + 8 (r >> 1) of sub-tile u).
+  auto finish = [&](int i, int t, int b, int total) {
+    const int e = threadIdx.x + kConsumerThreads * i;
+    const int m = 8 * ((e >> 7) % NT8) + 2 * (e & 3) + ((e >> 5) & 1);
+    const int nl = 16 * ((e >> 7) / NT8) + ((e & 31) >> 2) + 8 * ((e >> 6) & 1);
+    store_out(p, m, t * kTileRows + nl, total, xs_sm[m], ws_sm[b][nl]);
+  };
+  // A split segment whose atomics are in flight: tile, sum buffer, contributor count, results.
+  bool pending = false;
+  int pend_t = 0, pend_buf = 0;
+  uint32_t pend_n = 0;
+  unsigned long long pend_old[kPer];
+  auto resolve = [&]() {
+    int* const pm = segsum + pend_buf * kSegInts + threadIdx.x;
+    unsigned long long* const tacc = p.tile_acc + (size_t)pend_t * kSegInts + threadIdx.x;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const uint32_t arrived = (uint32_t)(pend_old[i] >> 52);
+      const uint32_t biased = (uint32_t)pm[kConsumerThreads * i] ^ 0x80000000u;
+      pm[kConsumerThreads * i] = 0;
+      if (arrived == pend_n - 1) {
+        tacc[kConsumerThreads * i] = 0ull;
+        // the biased sum minus n * 2^31, mod 2^32
+        finish(i, pend_t, pend_buf, (int)((uint32_t)pend_old[i] + biased - ((pend_n & 1u) << 31)));
+      } else if (arrived >= pend_n) {
+        atomicOr(p.status, W8A8_DEV_COUNTER_CORRUPT);
+      }
+    }
+    pending = false;
+  };
+
   for (StageIter it(b0, b1, p.KB, kStageSlabs); !it.done(); it.next(), ++q) {
     const int s = q % NS;
     if (it.u == it.seg_begin) {
       // Start of a segment: count the tile's contributors now, off the segment's tail.
       const long long t = it.t;
       arrivals = (uint32_t)(split_owner((t + 1) * p.KB - 1, p.U, p.G) - split_owner(t * p.KB, p.U, p.G) + 1);
+      const int n = it.t * kTileRows + (int)threadIdx.x;
+      if (threadIdx.x < kTileRows) ws_reg = n < p.N ? __ldg(p.w_scale + n) : 0.f;
     }
     if (kHalfSubTiles || (q & 1) == half) {
       if (!mbar_wait(&full_bar[s], (uint32_t)((q / NS) & 1), &abort_flag, p.status)) return;
@@ -325,43 +369,27 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
     if (!it.last_of_segment()) continue;
 
     // ------------------------------------------------------------ end of this CTA's part of a tile
-    // Element e = threadIdx.x + kConsumerThreads * i of the segment sums (layout [sub][j][r][lane])
-    // is this thread's i-th output element.  Its scales are prefetched into L1 first, so that
-    // their latency hides behind the flush and the barrier.
-    const int n_tile = it.t * kTileRows;
-    // Row m and column n of element e: the inverse of frag_index and of the accumulator fragment
-    // (lane = 4g + c holds rows 2c + (r & 1) of n8 tile j and columns g + 8 (r >> 1) of sub-tile u).
-    auto elem_m = [&](int i) {
-      const int e = threadIdx.x + kConsumerThreads * i;
-      return 8 * ((e >> 7) % NT8) + 2 * (e & 3) + ((e >> 5) & 1);
-    };
-    auto elem_n = [&](int i) {
-      const int e = threadIdx.x + kConsumerThreads * i;
-      return n_tile + 16 * ((e >> 7) / NT8) + ((e & 31) >> 2) + 8 * ((e >> 6) & 1);
-    };
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int m = elem_m(i), n = elem_n(i);
-      if (m < p.M) prefetch_l1(p.x_scale + m);
-      if (n < p.N) prefetch_l1(p.w_scale + n);
-    }
-    int* const sums = segsum + (segs & 1) * kSegInts;
+    const int buf = segs & 1;
+    if (threadIdx.x < 32 && segs == 0) xs_sm[threadIdx.x] = xs_reg;
+    if (threadIdx.x < kTileRows) ws_sm[buf][threadIdx.x] = ws_reg;
+    int* const sums = segsum + buf * kSegInts;
     if (since) flush(sums);
     since = 0;
     ++segs;
-    // Every consumer's part is in the sums.  The buffer is next written two segments later, after
-    // the next segment's barrier, which each thread reaches only after its reads and clears here.
+    // The previous split segment's atomics were issued one segment ago: their results are back.
+    // Its sum buffer and scales stay untouched until after the barrier below.
+    if (pending) resolve();
+    // Every consumer's part is in the sums, and the scales are in shared memory.  Both buffers are
+    // next written two segments later, after the next segment's barrier, which each thread reaches
+    // only after its reads and clears here (a split segment's reads and clears happen at the next
+    // segment end, before that barrier, or after the loop).
     named_bar_sync(kSegmentBarrier, kConsumerThreads);
     const int t = it.t;
     int* const mine = sums + threadIdx.x;   // element i at mine[kConsumerThreads * i]
-    auto finish = [&](int i, int total) {    // scales were prefetched into L1 above
-      const int m = elem_m(i), n = elem_n(i);
-      store_out(p, m, n, total, m < p.M ? __ldg(p.x_scale + m) : 0.f, n < p.N ? __ldg(p.w_scale + n) : 0.f);
-    };
     if (it.seg_begin == t * p.KB && it.seg_end == (t + 1) * p.KB) {   // the whole tile is ours
 #pragma unroll
       for (int i = 0; i < kPer; ++i) {
-        finish(i, mine[kConsumerThreads * i]);
+        finish(i, t, buf, mine[kConsumerThreads * i]);
         mine[kConsumerThreads * i] = 0;
       }
       continue;
@@ -371,27 +399,20 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
     // CTAs share a tile, so neither field overflows).  int32 addition is associative, so the CTA
     // that brings the count to n holds the same total, in the same bits, as an ascending-order
     // sum of the n partials; it stores the bf16 result and returns the word to zero for the next
-    // call.  One returning atomic per element: no separate counter, fence or read-back.
-    const uint32_t n = arrivals;
+    // call.  One returning atomic per element: no separate counter, fence or read-back.  The
+    // results are examined one segment later (or after the last one), so the consumers go on
+    // streaming while the atomics travel.
     unsigned long long* const tacc = p.tile_acc + (size_t)t * kSegInts + threadIdx.x;
-    unsigned long long old[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; ++i)
-      old[i] = atom_add_relaxed_u64(tacc + kConsumerThreads * i,
-                                    (1ull << 52) + ((uint32_t)mine[kConsumerThreads * i] ^ 0x80000000u));
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const uint32_t arrived = (uint32_t)(old[i] >> 52);
-      const uint32_t biased = (uint32_t)mine[kConsumerThreads * i] ^ 0x80000000u;
-      mine[kConsumerThreads * i] = 0;
-      if (arrived == n - 1) {
-        tacc[kConsumerThreads * i] = 0ull;
-        finish(i, (int)((uint32_t)old[i] + biased - ((n & 1u) << 31)));   // biased sum - n * 2^31, mod 2^32
-      } else if (arrived >= n) {
-        atomicOr(p.status, W8A8_DEV_COUNTER_CORRUPT);
-      }
-    }
+      pend_old[i] = atom_add_relaxed_u64(tacc + kConsumerThreads * i,
+                                         (1ull << 52) + ((uint32_t)mine[kConsumerThreads * i] ^ 0x80000000u));
+    pending = true;
+    pend_t = t;
+    pend_buf = buf;
+    pend_n = arrivals;
   }
+  if (pending) resolve();
 }
 
 // --------------------------------------------------------------------------------------------
@@ -420,35 +441,6 @@ static size_t gemm_smem_bytes(int nt8) {
 
 static constexpr int kAutoCtasPerSm = 2;   // resident CTAs per SM (shared memory and registers)
 
-// Automatic CTA count.  More CTAs stream the weight faster, but every split tile adds one partial
-// per CTA that shares it, and the partials meet in the L2 atomic units at the end of the call
-// (measured: about 22.5 ps per partial value when all CTAs finish together).  Measured stream
-// rates: a CTA alone on its SM about 25 GB/s; two CTAs on every SM about 20 GB/s each, and the
-// whole part about 6 TB/s.  CTA counts between one and two per SM leave the SMs that hold two
-// CTAs as the slowest, so the candidates are up to one CTA per SM (multiples of an eighth of the
-// SM count) and exactly two per SM; the plan takes the lowest modelled time.
-static int auto_blocks(long long slabs, int n_tiles, int nt8, int sm_count) {
-  const double weight_bytes = (double)slabs * kSlabBytes;
-  const double sec_per_partial = 22.5e-12;
-  const int sms = sm_count > 0 ? sm_count : 152;
-  int best = 0;
-  double best_t = 0.0;
-  for (int k = 4; k <= 9; ++k) {
-    const long long g = k <= 8 ? (long long)k * sms / 8 : (long long)kAutoCtasPerSm * sms;
-    if (g < 1 || g > slabs) continue;
-    double rate = k <= 8 ? (double)g * 25e9 : (double)g * 20e9;
-    if (rate > 6.0e12) rate = 6.0e12;
-    // Split segments that finish together at the end: with at least as many CTAs as tiles every
-    // tile is cut (about g + n_tiles segments, all ending with the runs); with fewer, each CTA's
-    // last segment (the first one ends early and its partial overlaps the stream).
-    const double split_segments = (double)(g >= n_tiles ? g + n_tiles : g);
-    const double t = weight_bytes / rate + sec_per_partial * 512.0 * nt8 * split_segments;
-    if (best == 0 || t < best_t) best = (int)g, best_t = t;
-  }
-  if (best == 0) best = (int)(slabs < (long long)kAutoCtasPerSm * sms ? slabs : (long long)kAutoCtasPerSm * sms);
-  return best;
-}
-
 int gemm_plan(int M, int K, int N, int blocks, int sm_count, GemmPlan* plan) {
   if (M < 1 || M > 32 || K < 1 || K > 65536 || N < 1 || N > 1048576 || blocks < 0) return W8A8_ERR_INVALID_ARG;
   if (K % 32 != 0 || N % 8 != 0) return W8A8_ERR_UNSUPPORTED_SHAPE;
@@ -458,7 +450,10 @@ int gemm_plan(int M, int K, int N, int blocks, int sm_count, GemmPlan* plan) {
   pl.kb = K / kKBlock;
   pl.slabs = (long long)pl.n_tiles * pl.kb;
   if (blocks == 0) {
-    pl.blocks = auto_blocks(pl.slabs, pl.n_tiles, pl.nt8, sm_count);
+    // Two CTAs on every SM: measured fastest for every workload shape once the split-tile
+    // combine costs one round trip (fewer CTAs stream slower and save little in the combine).
+    const long long g = (long long)kAutoCtasPerSm * (sm_count > 0 ? sm_count : 152);
+    pl.blocks = (int)(g < pl.slabs ? g : pl.slabs);
   } else {
     if (blocks > pl.slabs) return W8A8_ERR_INVALID_ARG;
     pl.blocks = blocks;
