@@ -10,8 +10,8 @@
 namespace w8a8 {
 
 // A pipeline wait gives up after this many SM clock cycles (about one second at GB300 clocks) and
-// reports W8A8_DEV_WAIT_TIMEOUT instead of spinning forever.  The cycle counter is cheap to read;
-// it is consulted only every 64 unsuccessful polls.
+// reports W8A8_DEV_WAIT_TIMEOUT instead of spinning forever.  The cycle counter is read once per
+// suspended poll (each poll sleeps at most kSuspendHintNs).
 constexpr long long kWaitTimeoutCycles = 2000000000ll;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -46,6 +46,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same, but a thread whose phase is not complete stays suspended (issuing nothing) until the
+// phase completes or about kSuspendHintNs have passed, instead of returning at once: waiting warps
+// then leave the issue slots to the warps that have work.
+constexpr uint32_t kSuspendHintNs = 20000;
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase of `parity` to complete.  Bounded: gives up when another thread of the CTA
 // has raised *abort, or after kWaitTimeoutCycles (then records the timeout in *status and raises
 // *abort).  Returns true when the phase completed.
@@ -53,15 +67,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
                                           uint32_t* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  for (unsigned it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*abort) return false;
-      if (clock64() - t0 > kWaitTimeoutCycles) {
-        atomicOr(status, W8A8_DEV_WAIT_TIMEOUT);
-        *abort = 1;
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > kWaitTimeoutCycles) {
+      atomicOr(status, W8A8_DEV_WAIT_TIMEOUT);
+      *abort = 1;
+      return false;
     }
   }
 }
@@ -70,9 +82,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // only.  Returns false on timeout (recorded in *status).
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint32_t* status) {
   const long long t0 = clock64();
-  for (unsigned it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u && clock64() - t0 > kWaitTimeoutCycles) {
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity)) return true;
+    if (clock64() - t0 > kWaitTimeoutCycles) {
       atomicOr(status, W8A8_DEV_WAIT_TIMEOUT);
       return false;
     }
@@ -206,6 +218,92 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_u32(uint32_t* addr, uint32_
   uint32_t old;
   asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
   return old;
+}
+
+}  // namespace w8a8
+
+namespace w8a8 {
+
+// ---------------------------------------------------------------- fifth-generation tensor cores
+// tcgen05 instructions (one CTA, cta_group::1).  Tensor memory addresses carry the lane in bits
+// 31..16 and the 32-bit column in bits 15..0; a warp reaches lanes 32 * (warp % 4) ... + 31.
+
+// Allocate `cols` tensor-memory columns (a power of two >= 32); the whole warp executes it and the
+// base address lands in *dst (shared memory).
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst)), "r"(cols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t base, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(cols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Generic-proxy shared-memory writes become visible to the tensor core (async proxy).
+__device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: no swizzle, K-major.  Core matrix = 8 rows x 16 bytes; for a
+// 16-bit operand, element (row r, k) sits at (r / 8) * sbo + (k / 8) * lbo + (r % 8) * 16 + (k % 8) * 2
+// from the start address.  Bits 46..47 hold the descriptor version of this architecture (1).
+__device__ __forceinline__ uint64_t smem_desc_kmajor(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
+}
+
+// Instruction descriptor of kind::f16: D f32 (bits 4..5 = 1), A and B f16 (0), both K-major,
+// N / 8 in bits 17..22, M / 16 in bits 24..28.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem_d] (+)= A[tmem_a] * B[desc_b]^T, A from tensor memory (lane = row, column c = the f16 pair
+// k = 2c, 2c + 1), B from shared memory.  Issued by one thread.
+__device__ __forceinline__ void umma_f16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t desc_b, uint32_t idesc,
+                                                bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(
+          tmem_d),
+      "r"(tmem_a), "l"(desc_b), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+// 16 consecutive columns of this thread's lane, written / read (warp-wide).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Four int8 values in offset binary, bytes in natural order (b0, b1, b2, b3) -> the fp16 pairs
+// (b0, b1) and (b2, b3) (first element in the low half), exactly (see offset_bytes_to_half2).
+__device__ __forceinline__ void offset_bytes_to_half2_pairs(uint32_t u, uint32_t& p01, uint32_t& p23) {
+  const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
+  const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+  __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+  __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+  p01 = *reinterpret_cast<uint32_t*>(&ha);
+  p23 = *reinterpret_cast<uint32_t*>(&hb);
 }
 
 }  // namespace w8a8

@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
       for (int r = 0; r < 4; ++r) facc[u][j][r] = 0.f;
   int since = 0;          // slabs accumulated in fp32 by this warp since its last flush
   int segs = 0;
-  int q = 0;
+  int q = 0;              // CTA-wide stage index of the current segment's first stage
   uint32_t arrivals = 0;  // CTAs whose runs share the current segment's tile
   // Scales are fetched into registers long before they are needed (x_scale at the start, a
   // tile's w_scale at the start of its segment) and parked in shared memory just before the
@@ -314,30 +314,44 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
     pending = false;
   };
 
-  for (StageIter it(b0, b1, p.KB, kStageSlabs); !it.done(); it.next(), ++q) {
-    const int s = q % NS;
-    if (it.u == it.seg_begin) {
-      // Start of a segment: count the tile's contributors now, off the segment's tail.
-      const long long t = it.t;
-      arrivals = (uint32_t)(split_owner((t + 1) * p.KB - 1, p.U, p.G) - split_owner(t * p.KB, p.U, p.G) + 1);
-      const int n = it.t * kTileRows + (int)threadIdx.x;
-      if (threadIdx.x < kTileRows) ws_reg = n < p.N ? __ldg(p.w_scale + n) : 0.f;
+  // Offsets of this warp's fragments inside a stage (the same for every stage): W fragments of
+  // its sub-tiles in its slab; row g of the activation box sits at g * 128 with its 16-byte chunks
+  // XOR-swizzled by g, and n8 tile j adds j * 1024.
+  const int w_off = slab * kSlabBytes + sub0 * 512 + lane * 16;
+  const int x_off = g * 128 + (((2 * slab + (c >> 1)) ^ g) << 4) + 8 * (c & 1);
+  constexpr int kStep = kHalfSubTiles ? 1 : 2;   // stages from one of this warp's stages to the next
+
+  // The run [b0, b1) is walked segment by segment (one tile's part each); a segment of n slabs is
+  // ceil(n / 4) stages of the CTA-wide stage sequence, the last one possibly partial.  q is the
+  // CTA-wide index of the segment's first stage; this warp visits only its own stages.
+  for (int seg_begin = b0, seg_end = 0; seg_begin < b1; seg_begin = seg_end) {
+    const int t = seg_begin / p.KB;
+    seg_end = min(b1, (t + 1) * p.KB);
+    const int seg_slabs = seg_end - seg_begin;
+    const int seg_stages = (seg_slabs + kStageSlabs - 1) / kStageSlabs;
+    // Start of a segment: count the tile's contributors and fetch its w_scale now, off the
+    // segment's tail.
+    arrivals = (uint32_t)(split_owner((long long)(t + 1) * p.KB - 1, p.U, p.G) -
+                          split_owner((long long)t * p.KB, p.U, p.G) + 1);
+    if (threadIdx.x < kTileRows) {
+      const int n = t * kTileRows + (int)threadIdx.x;
+      ws_reg = n < p.N ? __ldg(p.w_scale + n) : 0.f;
     }
-    if (kHalfSubTiles || (q & 1) == half) {
-      if (!mbar_wait(&full_bar[s], (uint32_t)((q / NS) & 1), &abort_flag, p.status)) return;
-      if (slab < it.ns) {
+    for (int i = kHalfSubTiles ? 0 : ((half - q) & 1); i < seg_stages; i += kStep) {
+      const int qs = q + i;
+      const int s = qs % NS;
+      if (!mbar_wait(&full_bar[s], (uint32_t)((qs / NS) & 1), &abort_flag, p.status)) return;
+      if (slab < seg_slabs - kStageSlabs * i) {
         // Weight fragments of this warp's sub-tiles, then this slab's activation B fragments.
-        const uint8_t* wst = wring + s * L::kWStage + slab * kSlabBytes + sub0 * 512 + lane * 16;
+        const uint8_t* wst = wring + s * L::kWStage + w_off;
         uint4 w[kWarpSubTiles];
 #pragma unroll
         for (int u = 0; u < kWarpSubTiles; ++u) w[u] = *reinterpret_cast<const uint4*>(wst + u * 512);
-        // Row m of the box sits at m * 128 with its 16-byte chunks XOR-swizzled by (m & 7) = g.
-        const uint8_t* xr = xraw + s * L::kXRawStage;
-        const int chunk = 2 * slab + (c >> 1);
+        const uint8_t* xr = xraw + s * L::kXRawStage + x_off;
         uint32_t b[NT8][4];
 #pragma unroll
         for (int j = 0; j < NT8; ++j) {
-          const uint2 v = *reinterpret_cast<const uint2*>(xr + (8 * j + g) * 128 + ((chunk ^ g) << 4) + 8 * (c & 1));
+          const uint2 v = *reinterpret_cast<const uint2*>(xr + j * 1024);
           offset_bytes_to_half2(v.x ^ 0x80808080u, b[j][0], b[j][1]);
           offset_bytes_to_half2(v.y ^ 0x80808080u, b[j][2], b[j][3]);
         }
@@ -347,26 +361,31 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
           flush(segsum + (segs & 1) * kSegInts);
           since = 0;
         }
+        // Convert every weight fragment first, then issue the MMAs k-step by k-step, so that the
+        // two MMAs into one accumulator are a whole k-step's worth of independent MMAs apart.
+        uint32_t a[kWarpSubTiles][2][4];
 #pragma unroll
         for (int u = 0; u < kWarpSubTiles; ++u) {
-          uint32_t a[2][4];
-          offset_bytes_to_half2(w[u].x, a[0][0], a[0][2]);   // row g,   k 8c+0..3
-          offset_bytes_to_half2(w[u].y, a[0][1], a[0][3]);   // row g+8, k 8c+0..3
-          offset_bytes_to_half2(w[u].z, a[1][0], a[1][2]);   // row g,   k 8c+4..7
-          offset_bytes_to_half2(w[u].w, a[1][1], a[1][3]);   // row g+8, k 8c+4..7
+          offset_bytes_to_half2(w[u].x, a[u][0][0], a[u][0][2]);   // row g,   k 8c+0..3
+          offset_bytes_to_half2(w[u].y, a[u][0][1], a[u][0][3]);   // row g+8, k 8c+0..3
+          offset_bytes_to_half2(w[u].z, a[u][1][0], a[u][1][2]);   // row g,   k 8c+4..7
+          offset_bytes_to_half2(w[u].w, a[u][1][1], a[u][1][3]);   // row g+8, k 8c+4..7
+        }
 #pragma unroll
-          for (int st = 0; st < 2; ++st)
+        for (int st = 0; st < 2; ++st)
+#pragma unroll
+          for (int u = 0; u < kWarpSubTiles; ++u)
 #pragma unroll
             for (int j = 0; j < NT8; ++j)
-              mma_f16_16816(facc[u][j], a[st][0], a[st][1], a[st][2], a[st][3], b[j][2 * st], b[j][2 * st + 1]);
-        }
+              mma_f16_16816(facc[u][j], a[u][st][0], a[u][st][1], a[u][st][2], a[u][st][3], b[j][2 * st],
+                            b[j][2 * st + 1]);
         ++since;
       } else {
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
       }
     }
-    if (!it.last_of_segment()) continue;
+    q += seg_stages;
 
     // ------------------------------------------------------------ end of this CTA's part of a tile
     const int buf = segs & 1;
@@ -384,9 +403,8 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
     // only after its reads and clears here (a split segment's reads and clears happen at the next
     // segment end, before that barrier, or after the loop).
     named_bar_sync(kSegmentBarrier, kConsumerThreads);
-    const int t = it.t;
     int* const mine = sums + threadIdx.x;   // element i at mine[kConsumerThreads * i]
-    if (it.seg_begin == t * p.KB && it.seg_end == (t + 1) * p.KB) {   // the whole tile is ours
+    if (seg_begin == t * p.KB && seg_end == (t + 1) * p.KB) {   // the whole tile is ours
 #pragma unroll
       for (int i = 0; i < kPer; ++i) {
         finish(i, t, buf, mine[kConsumerThreads * i]);
