@@ -472,6 +472,32 @@ def run_sweep(args):
                 print(json.dumps(time_q8(T, K8, N8, flags=flags)), flush=True)
 
 
+def run_ncu_driver(args):
+    """Profiling driver (for ncu captures, not a bench line): the default workload's public-API
+    calls, eagerly, on rotating packed weights (each call reads a different weight copy), then exit."""
+    import torch
+
+    import int8_weight_gemm_gb300 as lib8
+    import synth
+
+    cfg = DEFAULT
+    M, K, N = cfg["M"], cfg["K"], cfg["N"]
+    x, xs, W, ws = synth.w8a8_inputs(M, K, N, seed=cfg["seed"], dist=cfg["dist"])
+    dev = torch.device("cuda")
+    xd, xsd, wsd = (torch.from_numpy(a).to(dev) for a in (x, xs, ws))
+    wsp = lib8.alloc_workspace(lib8.w8a8_workspace_bytes(M, K, N), dev)
+    packed = lib8.w8a8_pack_weights(torch.from_numpy(W).to(dev), ws=wsp)
+    packs = [packed] + [packed.clone() for _ in range(7)]
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    for i in range(args.ncu_driver):
+        lib8.w8a8_gemm(xd, xsd, packs[i % len(packs)], wsd, wsp, N, out=out)
+    torch.cuda.synchronize()
+    status = lib8.w8a8_workspace_status(wsp)
+    print(json.dumps({"ncu_driver_calls": args.ncu_driver, "device_status": status}))
+    if status != 0:
+        sys.exit(1)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -484,10 +510,14 @@ def main():
     ap.add_argument("--shapes", default="", help="comma list of sweep shape indices (default: all)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-q8", action="store_true", help="skip the Q8_0 timings")
+    ap.add_argument("--ncu-driver", type=int, default=0,
+                    help="profiling driver: this many eager calls of the default workload, then exit")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.impl == "reference":
+    if args.ncu_driver:
+        run_ncu_driver(args)
+    elif args.impl == "reference":
         run_reference(args)
     elif args.sweep:
         run_sweep(args)
