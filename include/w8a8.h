@@ -131,10 +131,13 @@ int w8a8_pack_weights(const int8_t* W, int K, int N, void* W_packed, void* ws, s
  *  out      [M,N] bf16 row-major (uint16_t storage), 16-byte aligned; rows m >= M and columns
  *           n >= N are never written.
  *  M in [1, 32]; K % 32 == 0; N % 8 == 0 (same limits as the pack).
- *  blocks   number of CTAs that share the (N/64 tiles) x (K/32 blocks) work as equal contiguous
- *           runs of 2-KiB slabs (split-K generalised: a tile's K range is cut wherever a CTA's run
- *           starts or ends; every cut lies on a 32-aligned k).  0 = automatic (a multiple of
- *           the SM count).  Must not exceed the number of slabs.
+ *  blocks   number of CTAs that share the T = ceil(N/64) tiles x KB = K/32 slabs of 2 KiB
+ *           (split-K generalised; every cut lies on a 32-aligned k).  With blocks >= T each tile
+ *           is cut into c + 1 (the first blocks % T tiles) or c = blocks / T contiguous parts of
+ *           equal length to within one slab, one per CTA, so no CTA spans two tiles; with
+ *           blocks < T the tiles are laid end to end and CTA i takes a contiguous run of
+ *           ceil or floor(T KB / blocks) slabs (the longer runs first).  0 = automatic (twice
+ *           the SM count, at most one CTA per slab).  Must not exceed the number of slabs.
  *  flags    0 or W8A8_FLAG_PDL; any other bit is INVALID_ARG.
  *  ws       workspace of at least w8a8_workspace_bytes(M, K, N, blocks) bytes.
  *  The int32 sums are exact (the result does not depend on `blocks`), and the epilogue order is
@@ -160,9 +163,9 @@ typedef struct {
 
 int w8a8_plan(int M, int K, int N, int blocks, w8a8_plan_t* plan);
 
-/* The slab runs of a plan: bounds[i] = first slab of CTA i, bounds[blocks] = total slabs
- * (slab u covers tile u / KB, k in [32 (u % KB), 32 (u % KB) + 32)).  n_bounds must be
- * blocks + 1.  Host-only. */
+/* The slab runs of a plan (the split described at w8a8_gemm's `blocks`): bounds[i] = first
+ * slab of CTA i, bounds[blocks] = total slabs (slab u covers tile u / KB, k in
+ * [32 (u % KB), 32 (u % KB) + 32)).  n_bounds must be blocks + 1.  Host-only. */
 int w8a8_split_bounds(int K, int N, int blocks, long long* bounds, int n_bounds);
 
 /* W8A8 decode GEMM that allocates nothing and takes no workspace.  The pages have no counterpart:

@@ -171,7 +171,13 @@ int w8a8_split_bounds(int K, int N, int blocks, long long* bounds, int n_bounds)
   int rc = gemm_plan(1, K, N, blocks, current_sm_count(), &pl);
   if (rc != W8A8_OK) return rc;
   if (n_bounds != pl.blocks + 1) return W8A8_ERR_INVALID_ARG;
-  for (int i = 0; i <= pl.blocks; ++i) bounds[i] = split_lo(i, pl.slabs, pl.blocks);
+  const GemmSplit sp = make_gemm_split(pl.n_tiles, pl.kb, pl.blocks);
+  for (int i = 0; i < pl.blocks; ++i) {
+    int b0, b1;
+    gemm_split_run(sp, i, &b0, &b1);
+    bounds[i] = b0;
+  }
+  bounds[pl.blocks] = pl.slabs;
   return W8A8_OK;
 }
 

@@ -160,15 +160,76 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// ---------------------------------------------------------------- split plan (host and device)
-// CTA i of G owns slabs [split_lo(i), split_lo(i+1)) of U: equal runs within one slab.
-__host__ __device__ __forceinline__ long long split_lo(long long i, long long U, long long G) {
-  return i * U / G;
+// ---------------------------------------------------------------- split plans (host and device)
+// Part i of G equal parts of [0, U): [even_lo(i), even_lo(i + 1)), runs within one of each other.
+// 32-bit arithmetic only (i * U < 2^31 at every call site): a 64-bit division is a called
+// subroutine on the GPU, and in a kernel prologue its latency delays the first copy.
+__host__ __device__ __forceinline__ int even_lo(int i, int U, int G) {
+  return (int)((unsigned)(i * U) / (unsigned)G);
 }
 
-// The CTA whose run contains slab u (requires G <= U, so that no run is empty).
-__host__ __device__ __forceinline__ long long split_owner(long long u, long long U, long long G) {
-  return ((u + 1) * G + U - 1) / U - 1;
+// Work split of a W8A8 GEMM call: G CTAs share T tiles of KB slabs (U = T * KB slabs, U < 2^31).
+//  - Tile-aligned (G >= T): tile t is cut into P_t parts, P_t = c + 1 for the first e tiles and
+//    c for the rest (c = G / T, e = G % T), part j of P_t taking slabs [even_lo(j), even_lo(j+1))
+//    of the tile's KB.  No CTA crosses a tile, so each CTA finishes exactly one tile segment and
+//    P_t CTAs meet in the tile's combine.
+//  - Linear (G < T): the tiles are laid end to end and CTA i takes a contiguous run of a + 1
+//    (i < r) or a slabs (a = U / G, r = U % G), which may span several tiles.
+// Both cover every slab exactly once with no empty run (G <= U).
+struct GemmSplit {
+  int T, KB, G;
+  int aligned;
+  int c, e;   // tile-aligned: parts per tile, tiles with one extra part
+  int a, r;   // linear: run length, runs one slab longer
+};
+
+inline GemmSplit make_gemm_split(int T, int KB, int G) {
+  GemmSplit s{};
+  s.T = T;
+  s.KB = KB;
+  s.G = G;
+  s.aligned = G >= T;
+  s.c = G / T;
+  s.e = G % T;
+  const int U = T * KB;
+  s.a = U / G;
+  s.r = U % G;
+  return s;
+}
+
+// First and one-past-last slab of CTA i.
+__host__ __device__ __forceinline__ void gemm_split_run(const GemmSplit& s, int i, int* b0, int* b1) {
+  if (s.aligned) {
+    const int big = s.e * (s.c + 1);   // CTAs of the tiles cut into c + 1 parts
+    int t, j, P;
+    if (i < big) {
+      P = s.c + 1;
+      t = (int)((unsigned)i / (unsigned)P);
+      j = i - t * P;
+    } else {
+      P = s.c;
+      const int tt = (int)((unsigned)(i - big) / (unsigned)P);
+      t = s.e + tt;
+      j = i - big - tt * P;
+    }
+    *b0 = t * s.KB + even_lo(j, s.KB, P);
+    *b1 = t * s.KB + even_lo(j + 1, s.KB, P);
+  } else {
+    *b0 = i * s.a + (i < s.r ? i : s.r);
+    *b1 = *b0 + s.a + (i < s.r ? 1 : 0);
+  }
+}
+
+// The CTA whose run contains slab u (linear split).
+__host__ __device__ __forceinline__ int gemm_split_owner_linear(const GemmSplit& s, int u) {
+  const int head = s.r * (s.a + 1);   // slabs of the longer runs
+  return u < head ? (int)((unsigned)u / (unsigned)(s.a + 1)) : s.r + (int)((unsigned)(u - head) / (unsigned)s.a);
+}
+
+// Number of CTAs whose runs share tile t (the tile's combine waits for this many partials).
+__host__ __device__ __forceinline__ int gemm_split_contributors(const GemmSplit& s, int t) {
+  if (s.aligned) return t < s.e ? s.c + 1 : s.c;
+  return gemm_split_owner_linear(s, t * s.KB + s.KB - 1) - gemm_split_owner_linear(s, t * s.KB) + 1;
 }
 
 }  // namespace w8a8

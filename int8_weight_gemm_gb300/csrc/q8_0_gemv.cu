@@ -60,10 +60,10 @@ __global__ void __launch_bounds__(32 * kQ8MaxWarps) q8_0_gemv_kernel(const __gri
   const int g = lane >> 2, c = lane & 3;
   const int tile = blockIdx.x / p.splits;
   const int split = blockIdx.x % p.splits;
-  const int cb0 = (int)split_lo(split, p.KB, p.splits);
-  const int cb1 = (int)split_lo(split + 1, p.KB, p.splits);
-  const int wb0 = cb0 + (int)split_lo(warp, cb1 - cb0, p.warps);
-  const int wb1 = cb0 + (int)split_lo(warp + 1, cb1 - cb0, p.warps);
+  const int cb0 = even_lo(split, p.KB, p.splits);
+  const int cb1 = even_lo(split + 1, p.KB, p.splits);
+  const int wb0 = cb0 + even_lo(warp, cb1 - cb0, p.warps);
+  const int wb1 = cb0 + even_lo(warp + 1, cb1 - cb0, p.warps);
   const int nb = wb1 - wb0;
   const int n_a = tile * 16 + g, n_b = n_a + 8;
 

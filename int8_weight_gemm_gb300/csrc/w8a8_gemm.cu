@@ -103,8 +103,7 @@ struct GemmParams {
   // [tile][sub-tile][n8 tile][fragment register][lane].
   unsigned long long* tile_acc;
   int M, K, N, KB;
-  long long U;
-  int G;
+  GemmSplit split;    // which slabs each CTA streams
   int pdl;            // launched with programmatic dependent launch: prefetch W before the wait
 };
 
@@ -149,6 +148,7 @@ __device__ __forceinline__ void store_out(const GemmParams& p, int m, int n, int
 }
 
 constexpr int kProducerWarp = kConsumerWarps;        // warp 8: lane 0 issues every copy
+constexpr int kProducerThread = 32 * kProducerWarp;
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kSegmentBarrier = 1;                   // named barrier of the consumer warps
 
@@ -179,7 +179,20 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
+  int b0, b1;
+  gemm_split_run(p.split, (int)blockIdx.x, &b0, &b1);
+
+  // The producer thread initialises the barriers and issues the first stages' copies before the
+  // CTA-wide barrier, so that the weight stream starts as early as the CTA does; the consumers
+  // meanwhile clear the segment sums.  Every copy of a stage lands on the stage's full barrier,
+  // which counts the weight and activation bytes together.
+  const uint32_t xbox = (uint32_t)L::kXRawStage;
+  StageIter it(b0, b1, p.KB, kStageSlabs);   // producer: the next stage to issue
+  int pq = 0;                                 // producer: stages issued so far
+  uint64_t policy = 0;
+  if (threadIdx.x == kProducerThread) {
+    tma_prefetch_desc(&p.xmap);
+    policy = policy_evict_first();
 #pragma unroll
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full_bar[s], 1);
@@ -187,51 +200,39 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
     }
     abort_flag = 0;
     mbar_fence_init();
+    // The packed weight is never written by the work this call depends on, so its first stages
+    // are requested at once; the activation boxes wait for the dependency when there is one.
+    for (; pq < NS && !it.done(); it.next(), ++pq) {
+      mbar_arrive_expect_tx(&full_bar[pq], (uint32_t)(it.ns * kSlabBytes) + xbox);
+      bulk_g2s_hint(wring + pq * L::kWStage, p.wp + (size_t)it.u * kSlabBytes, (uint32_t)(it.ns * kSlabBytes),
+                    &full_bar[pq], policy);
+      if (!p.pdl) tma_load_2d(xraw + pq * L::kXRawStage, &p.xmap, it.kb0() * kKBlock, 0, &full_bar[pq]);
+    }
   }
   for (int i = threadIdx.x; i < L::kSegSumInts; i += kThreads) segsum[i] = 0;
   __syncthreads();
   pdl_trigger();   // the next call on the stream may start its own weight prefetch
 
-  const int b0 = (int)split_lo(blockIdx.x, p.U, p.G);
-  const int b1 = (int)split_lo(blockIdx.x + 1, p.U, p.G);
-
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- producer (one thread)
-    if (lane != 0) return;
-    tma_prefetch_desc(&p.xmap);
-    const uint64_t policy = policy_evict_first();
-    const uint32_t xbox = (uint32_t)L::kXRawStage;
-    StageIter it(b0, b1, p.KB, kStageSlabs);
-    int q = 0;
+    if (threadIdx.x != kProducerThread) return;
+    pdl_wait();
     if (p.pdl) {
-      // The packed weight is never written by the work this call depends on: start streaming it
-      // before the dependency wait, then add the activation boxes once the wait has returned.
-      StageIter pre = it;
-      int npre = 0;
-      while (npre < NS && !pre.done()) {
-        mbar_arrive_expect_tx(&full_bar[npre], (uint32_t)(pre.ns * kSlabBytes) + xbox);
-        bulk_g2s_hint(wring + npre * L::kWStage, p.wp + (size_t)pre.u * kSlabBytes, (uint32_t)(pre.ns * kSlabBytes),
-                      &full_bar[npre], policy);
-        pre.next();
-        ++npre;
-      }
-      pdl_wait();
-      for (; q < npre; ++q, it.next())
-        tma_load_2d(xraw + q * L::kXRawStage, &p.xmap, it.kb0() * kKBlock, 0, &full_bar[q]);
-    } else {
-      pdl_wait();
+      StageIter pre(b0, b1, p.KB, kStageSlabs);
+      for (int j = 0; j < pq; pre.next(), ++j)
+        tma_load_2d(xraw + j * L::kXRawStage, &p.xmap, pre.kb0() * kKBlock, 0, &full_bar[j]);
     }
-    for (; !it.done(); it.next(), ++q) {
-      const int s = q % NS;
-      if (q >= NS && !mbar_wait(&empty_bar[s], ((q / NS) & 1) ^ 1, &abort_flag, p.status)) break;
+    for (; !it.done(); it.next(), ++pq) {
+      const int s = pq % NS;
+      if (!mbar_wait(&empty_bar[s], ((pq / NS) & 1) ^ 1, &abort_flag, p.status)) break;
       mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(it.ns * kSlabBytes) + xbox);
       bulk_g2s_hint(wring + s * L::kWStage, p.wp + (size_t)it.u * kSlabBytes, (uint32_t)(it.ns * kSlabBytes), &full_bar[s],
                     policy);
       tma_load_2d(xraw + s * L::kXRawStage, &p.xmap, it.kb0() * kKBlock, 0, &full_bar[s]);
     }
     // Drain: every copy this thread issued must land before the CTA may exit.
-    for (int s = 0; s < NS && s < q; ++s) {
-      const int last = s + NS * ((q - 1 - s) / NS);
+    for (int s = 0; s < NS && s < pq; ++s) {
+      const int last = s + NS * ((pq - 1 - s) / NS);
       mbar_wait_drain(&full_bar[s], (uint32_t)((last / NS) & 1), p.status);
     }
     return;
@@ -331,8 +332,7 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
     const int seg_stages = (seg_slabs + kStageSlabs - 1) / kStageSlabs;
     // Start of a segment: count the tile's contributors and fetch its w_scale now, off the
     // segment's tail.
-    arrivals = (uint32_t)(split_owner((long long)(t + 1) * p.KB - 1, p.U, p.G) -
-                          split_owner((long long)t * p.KB, p.U, p.G) + 1);
+    arrivals = (uint32_t)gemm_split_contributors(p.split, t);
     if (threadIdx.x < kTileRows) {
       const int n = t * kTileRows + (int)threadIdx.x;
       ws_reg = n < p.N ? __ldg(p.w_scale + n) : 0.f;
@@ -530,8 +530,7 @@ cudaError_t gemm_launch(const GemmPlan& pl, const int8_t* x, const float* xs, co
   p.K = K;
   p.N = N;
   p.KB = pl.kb;
-  p.U = pl.slabs;
-  p.G = pl.blocks;
+  p.split = make_gemm_split(pl.n_tiles, pl.kb, pl.blocks);
   p.pdl = pdl ? 1 : 0;
   switch (pl.nt8) {
     case 1: return launch_gemm<1, kStages1>(p, pl.blocks, pdl, stream);

@@ -48,25 +48,50 @@ def test_packed_bytes_match_oracle_layout(K, N):
 
 
 @pytest.mark.parametrize("K,N,blocks", [(512, 256, 0), (4096, 1536, 0), (4096, 1536, 7), (4096, 24576, 0),
-                                        (64, 200, 0), (64, 200, 8), (12288, 4096, 304), (32, 8, 1)])
+                                        (64, 200, 0), (64, 200, 8), (12288, 4096, 304), (32, 8, 1),
+                                        (4096, 2560, 0), (2048, 4096, 0), (4096, 1536, 3072), (4096, 1536, 25),
+                                        (4096, 1536, 24), (4096, 1536, 23), (96, 136, 0)])
 def test_split_bounds_cover_every_slab_once(K, N, blocks):
     plan = lib8.w8a8_plan(1, K, N, blocks)
-    G, U, KB = plan["blocks"], plan["slabs"], plan["k_blocks"]
-    assert U == -(-N // 64) * (K // 32) and KB == K // 32
-    b = lib8.w8a8_split_bounds(K, N, G)
+    G, U, KB, T = plan["blocks"], plan["slabs"], plan["k_blocks"], plan["n_tiles"]
+    assert U == -(-N // 64) * (K // 32) == T * KB
+    b = np.array(lib8.w8a8_split_bounds(K, N, G))
     assert b[0] == 0 and b[-1] == U and len(b) == G + 1
     sizes = np.diff(b)
     assert (sizes >= 1).all()                         # no empty run (the combine relies on it)
-    assert sizes.max() - sizes.min() <= 1             # equal runs to within one slab
-    # Brute force: contributors of each tile from the runs, against the owner arithmetic the
-    # kernel uses (first CTA of the tile's first slab .. CTA of its last slab).
-    owner = np.searchsorted(np.array(b[1:]), np.arange(U), side="right")
-    for t in range(U // KB):
-        contrib = sorted(set(owner[t * KB:(t + 1) * KB].tolist()))
-        assert contrib == list(range(contrib[0], contrib[-1] + 1))
-        lo = ((t * KB + 1) * G + U - 1) // U - 1
-        hi = (((t + 1) * KB) * G + U - 1) // U - 1
-        assert (lo, hi) == (contrib[0], contrib[-1])
+    # Brute force: the CTAs whose runs touch each tile.
+    owner = np.searchsorted(b[1:], np.arange(U), side="right")
+    contrib = [sorted(set(owner[t * KB:(t + 1) * KB].tolist())) for t in range(T)]
+    for cs in contrib:
+        assert cs == list(range(cs[0], cs[-1] + 1))  # a tile's contributors are consecutive CTAs
+    if G >= T:
+        # Tile-aligned: no run crosses a tile, tile t has c + 1 parts if t < G % T else c, and the
+        # parts of one tile are equal to within one slab.
+        assert all(b0 // KB == (b1 - 1) // KB for b0, b1 in zip(b[:-1], b[1:]))
+        c, e = G // T, G % T
+        for t, cs in enumerate(contrib):
+            assert len(cs) == (c + 1 if t < e else c)
+            part = sizes[cs[0]:cs[-1] + 1]
+            assert part.max() - part.min() <= 1
+    else:
+        # Linear: runs of a + 1 slabs, then runs of a; the kernel counts a tile's contributors
+        # from the owners of its first and last slab with this arithmetic.
+        a, r = U // G, U % G
+        assert (sizes[:r] == a + 1).all() and (sizes[r:] == a).all()
+        def owner_of(u):
+            head = r * (a + 1)
+            return u // (a + 1) if u < head else r + (u - head) // a
+        for t, cs in enumerate(contrib):
+            assert owner_of(t * KB + KB - 1) - owner_of(t * KB) + 1 == len(cs)
+
+
+def test_automatic_split_keeps_every_cta_inside_one_tile_for_small_outputs():
+    # The fused-QKV-like shape: 24 tiles over 304 CTAs, 16 tiles cut 13 ways and 8 cut 12 ways,
+    # runs of 9 to 11 slabs, and no CTA finishing two tile segments.
+    b = np.array(lib8.w8a8_split_bounds(4096, 1536, 304))
+    sizes = np.diff(b)
+    assert sizes.min() == 9 and sizes.max() == 11
+    assert all(b0 // 128 == (b1 - 1) // 128 for b0, b1 in zip(b[:-1], b[1:]))
 
 
 def test_split_slices_reproduce_the_oracle_sums():
