@@ -159,6 +159,9 @@ typedef struct {
     int stages;            /* pipeline depth */
     size_t smem_bytes;     /* dynamic shared memory per CTA */
     size_t workspace_bytes;/* workspace this call needs */
+    int combine_pack_bits; /* split-tile combine: 0 = one output element per 64-bit workspace word,
+                              f > 0 = two elements per word in f-bit fields plus a 64 - 2f bit
+                              arrival count (chosen when both fit; halves the atomics) */
 } w8a8_plan_t;
 
 int w8a8_plan(int M, int K, int N, int blocks, w8a8_plan_t* plan);

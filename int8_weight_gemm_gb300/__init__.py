@@ -52,6 +52,7 @@ class PlanT(ctypes.Structure):
         ("stages", ctypes.c_int),
         ("smem_bytes", ctypes.c_size_t),
         ("workspace_bytes", ctypes.c_size_t),
+        ("combine_pack_bits", ctypes.c_int),
     ]
 
 

@@ -162,6 +162,7 @@ int w8a8_plan(int M, int K, int N, int blocks, w8a8_plan_t* plan) {
   plan->stages = pl.stages;
   plan->smem_bytes = pl.smem_bytes;
   plan->workspace_bytes = pl.workspace_bytes;
+  plan->combine_pack_bits = pl.pack_f;
   return W8A8_OK;
 }
 

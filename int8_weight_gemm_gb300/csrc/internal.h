@@ -15,6 +15,7 @@ struct GemmPlan {
   int nt8, n_tiles, kb;
   long long slabs;
   int blocks, threads, stage_slabs, stages;
+  int pack_f;   // split-tile combine: bits per element field of a two-element word (0: one per word)
   size_t smem_bytes, workspace_bytes, partials_offset;
 };
 

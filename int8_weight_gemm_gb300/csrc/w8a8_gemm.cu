@@ -19,8 +19,8 @@
 //    needs at M = 16 (measured: mma.sync s8 ~150 TOPS vs fp16 ~600 TFLOPS), so the int8 values
 //    are converted exactly to fp16 (every int8 is an fp16 integer) and multiplied on the fp16
 //    tensor path with fp32 accumulation.  Products are integers of magnitude <= 2^14 and a
-//    partial sum over at most 512 k stays <= 2^23, so every fp32 accumulator value is an exact
-//    integer; the fp32 partials are converted to int32 (exactly) at least every 512 k and summed
+//    partial sum over at most 256 k stays <= 2^22, so every fp32 accumulator value is an exact
+//    integer; the fp32 partials are converted to int32 (exactly) at least every 256 k and summed
 //    in int32.  The result is the int32 sum an int8 MMA would produce, bit for bit.
 //  * Weight rows are the MMA's M dimension (16 rows per warp) and the activation rows are its
 //    N dimension (n8 tiles), so M <= 8 wastes nothing on a 16-row MMA tile.
@@ -39,7 +39,7 @@ constexpr int kConsumerWarps = 8;                  // two per stage slot: even /
 constexpr int kWarpsPerStage = 4;                  // one slab of a stage each
 constexpr int kSubTiles = 4;                       // 16-row sub-tiles of a 64-row tile
 constexpr int kThreads = 32 * (kConsumerWarps + 1);   // + one producer warp
-constexpr int kFlushSlabs = 16;                    // 16 slabs of 32 k = 512 k per warp between int32 flushes
+constexpr int kFlushSlabs = 8;                     // 8 slabs of 32 k = 256 k per warp between int32 flushes
 
 constexpr int kStageSlabs = 4;                     // one slab per consumer warp per stage
 
@@ -92,19 +92,26 @@ __global__ void w8a8_pack_kernel(const int8_t* __restrict__ W, int K, int N, int
 // GEMM
 // --------------------------------------------------------------------------------------------
 struct GemmParams {
-  CUtensorMap xmap;   // x_q [M, K] int8, box 128 x (8 * NT8), 128-byte swizzle, zero fill past M
+  // What a CTA needs before its first copy comes first, in one 64-byte line of the parameter
+  // bank: each first touch of a line costs a constant-cache miss at launch.
   const uint8_t* wp;
+  GemmSplit split;    // which slabs each CTA streams
+  int KB;
+  int pdl;            // launched with programmatic dependent launch: prefetch W before the wait
+  int M, N;
+  CUtensorMap xmap;   // x_q [M, K] int8, box 128 x (8 * NT8), 128-byte swizzle, zero fill past M
   const float* x_scale;
   const float* w_scale;
   uint16_t* out;
   uint32_t* status;
-  // One 64-bit word per output element of every tile: (arrivals << 52) + sum of (partial + 2^31)
-  // over the CTAs that have added their partial so far; zero between calls.  Layout
-  // [tile][sub-tile][n8 tile][fragment register][lane].
+  // Split-tile combine words, zero between calls, layout [tile][sub-tile][n8 tile][fragment
+  // register][lane].  pack_f = 0: one element per word, (arrivals << 52) + the sum of
+  // (partial + 2^31).  pack_f = f > 0: elements e and e + half share the word of e, holding
+  // a + b * 2^f + arrivals * 2^(2f) in two's complement, which every partial sum of the tile keeps
+  // in range (see gemm_plan).
   unsigned long long* tile_acc;
-  int M, K, N, KB;
-  GemmSplit split;    // which slabs each CTA streams
-  int pdl;            // launched with programmatic dependent launch: prefetch W before the wait
+  int K;
+  int pack_f;
 };
 
 // Walks a CTA's run of slabs [b0, b1) as stages of at most SS slabs that never cross a tile.
@@ -137,6 +144,14 @@ __device__ __forceinline__ int frag_index(int u, int j, int r, int lane) {
   return ((u * NT8 + j) * 4 + r) * 32 + lane;
 }
 
+// An fp32 value that is an integer v with |v| <= 2^22 (a partial sum over at most 256 k) to
+// int32 without the conversion unit: v + 1.5 * 2^23 lies in [2^23, 2^24], where fp32 spacing is
+// 1, so the sum is exact and its bit pattern is 0x4B400000 + v (at the ends 2^23 and 2^24 as
+// well).  One FP add and one integer add instead of a cvt, which runs at a quarter of the rate.
+__device__ __forceinline__ int exact_float_to_int(float v) {
+  return __float_as_int(__fadd_rn(v, 12582912.0f)) - 0x4B400000;
+}
+
 // Epilogue of one output element: out[m][n] = bf16_rne((float(acc) * x_scale[m]) * w_scale[n]).
 __device__ __forceinline__ void store_out(const GemmParams& p, int m, int n, int acc, float xsv, float wsv) {
   if (m < p.M && n < p.N) {
@@ -150,7 +165,6 @@ __device__ __forceinline__ void store_out(const GemmParams& p, int m, int n, int
 constexpr int kProducerWarp = kConsumerWarps;        // warp 8: lane 0 issues every copy
 constexpr int kProducerThread = 32 * kProducerWarp;
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
-constexpr int kSegmentBarrier = 1;                   // named barrier of the consumer warps
 
 template <int NT8, int NS>
 __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_constant__ GemmParams p) {
@@ -169,6 +183,7 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
   __shared__ __align__(8) uint64_t empty_bar[NS];  // the stage's consumer warps took their slabs
   __shared__ float xs_sm[32];                      // x_scale (0 past M)
   __shared__ float ws_sm[2][kTileRows];            // w_scale of a segment's tile, by segment parity
+  __shared__ __align__(8) uint64_t seg_bar;        // every consumer warp finished the segment
   __shared__ int abort_flag;
 
   // 128B-swizzled TMA boxes need a 1 KiB aligned destination.
@@ -198,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], kStageWarps);
     }
+    mbar_init(&seg_bar, kConsumerWarps);
     abort_flag = 0;
     mbar_fence_init();
     // The packed weight is never written by the work this call depends on, so its first stages
@@ -276,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
       for (int j = 0; j < NT8; ++j)
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          atomicAdd(dst + frag_index<NT8>(sub0 + u, j, r, lane), __float2int_rn(facc[u][j][r]));
+          atomicAdd(dst + frag_index<NT8>(sub0 + u, j, r, lane), exact_float_to_int(facc[u][j][r]));
           facc[u][j][r] = 0.f;
         }
   };
@@ -299,17 +315,45 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
   auto resolve = [&]() {
     int* const pm = segsum + pend_buf * kSegInts + threadIdx.x;
     unsigned long long* const tacc = p.tile_acc + (size_t)pend_t * kSegInts + threadIdx.x;
+    if (p.pack_f) {
+      const int pf = p.pack_f;
+      // Element pair (i, i + kPer / 2) shares word i.  The old word holds the sums a, b of the
+      // partials added before this CTA's and their count c: a = the low f bits sign-extended,
+      // b = the next f bits sign-extended after removing a, c = the rest after removing b.
+      const unsigned long long mask = (1ull << pf) - 1ull;
+      const int sh = 64 - pf;
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const uint32_t arrived = (uint32_t)(pend_old[i] >> 52);
-      const uint32_t biased = (uint32_t)pm[kConsumerThreads * i] ^ 0x80000000u;
-      pm[kConsumerThreads * i] = 0;
-      if (arrived == pend_n - 1) {
-        tacc[kConsumerThreads * i] = 0ull;
-        // the biased sum minus n * 2^31, mod 2^32
-        finish(i, pend_t, pend_buf, (int)((uint32_t)pend_old[i] + biased - ((pend_n & 1u) << 31)));
-      } else if (arrived >= pend_n) {
-        atomicOr(p.status, W8A8_DEV_COUNTER_CORRUPT);
+      for (int i = 0; i < kPer / 2; ++i) {
+        const unsigned long long w = pend_old[i];
+        const long long a = (long long)((w & mask) << sh) >> sh;
+        const unsigned long long w1 = (w - (unsigned long long)a) >> pf;
+        const long long bb = (long long)((w1 & mask) << sh) >> sh;
+        const uint32_t arrived = (uint32_t)((w1 - (unsigned long long)bb) >> pf);
+        const int va = pm[kConsumerThreads * i];
+        const int vb = pm[kConsumerThreads * (i + kPer / 2)];
+        pm[kConsumerThreads * i] = 0;
+        pm[kConsumerThreads * (i + kPer / 2)] = 0;
+        if (arrived == pend_n - 1) {
+          tacc[kConsumerThreads * i] = 0ull;
+          finish(i, pend_t, pend_buf, (int)(a + va));
+          finish(i + kPer / 2, pend_t, pend_buf, (int)(bb + vb));
+        } else if (arrived >= pend_n) {
+          atomicOr(p.status, W8A8_DEV_COUNTER_CORRUPT);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const uint32_t arrived = (uint32_t)(pend_old[i] >> 52);
+        const uint32_t biased = (uint32_t)pm[kConsumerThreads * i] ^ 0x80000000u;
+        pm[kConsumerThreads * i] = 0;
+        if (arrived == pend_n - 1) {
+          tacc[kConsumerThreads * i] = 0ull;
+          // the biased sum minus n * 2^31, mod 2^32
+          finish(i, pend_t, pend_buf, (int)((uint32_t)pend_old[i] + biased - ((pend_n & 1u) << 31)));
+        } else if (arrived >= pend_n) {
+          atomicOr(p.status, W8A8_DEV_COUNTER_CORRUPT);
+        }
       }
     }
     pending = false;
@@ -402,7 +446,11 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
     // next written two segments later, after the next segment's barrier, which each thread reaches
     // only after its reads and clears here (a split segment's reads and clears happen at the next
     // segment end, before that barrier, or after the loop).
-    named_bar_sync(kSegmentBarrier, kConsumerThreads);
+    // The barrier is an mbarrier wait, bounded like every other wait (a warp that gave up on a
+    // timeout never arrives, and the others then give up too).
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&seg_bar);
+    if (!mbar_wait(&seg_bar, (uint32_t)((segs - 1) & 1), &abort_flag, p.status)) return;
     int* const mine = sums + threadIdx.x;   // element i at mine[kConsumerThreads * i]
     if (seg_begin == t * p.KB && seg_end == (t + 1) * p.KB) {   // the whole tile is ours
 #pragma unroll
@@ -421,10 +469,23 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
     // results are examined one segment later (or after the last one), so the consumers go on
     // streaming while the atomics travel.
     unsigned long long* const tacc = p.tile_acc + (size_t)t * kSegInts + threadIdx.x;
+    if (p.pack_f) {
+      const int pf = p.pack_f;
+      // Two elements per word: half as many atomics (their number, not contention, bounds the
+      // combine's time).
 #pragma unroll
-    for (int i = 0; i < kPer; ++i)
-      pend_old[i] = atom_add_relaxed_u64(tacc + kConsumerThreads * i,
-                                         (1ull << 52) + ((uint32_t)mine[kConsumerThreads * i] ^ 0x80000000u));
+      for (int i = 0; i < kPer / 2; ++i) {
+        const long long va = mine[kConsumerThreads * i];
+        const long long vb = mine[kConsumerThreads * (i + kPer / 2)];
+        const unsigned long long inc = (1ull << (2 * pf)) + ((unsigned long long)vb << pf) + (unsigned long long)va;
+        pend_old[i] = atom_add_relaxed_u64(tacc + kConsumerThreads * i, inc);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < kPer; ++i)
+        pend_old[i] = atom_add_relaxed_u64(tacc + kConsumerThreads * i,
+                                           (1ull << 52) + ((uint32_t)mine[kConsumerThreads * i] ^ 0x80000000u));
+    }
     pending = true;
     pend_t = t;
     pend_buf = buf;
@@ -475,6 +536,22 @@ int gemm_plan(int M, int K, int N, int blocks, int sm_count, GemmPlan* plan) {
   } else {
     if (blocks > pl.slabs) return W8A8_ERR_INVALID_ARG;
     pl.blocks = blocks;
+  }
+  // Two-element combine words when both fields and the arrival count fit: every partial sum of an
+  // element is at most K * 2^14 in magnitude (|x|, |w| <= 128), so a signed field of f bits with
+  // 2^(f-1) > K * 2^14 holds it, and the count needs 64 - 2f bits for the most CTAs sharing a tile.
+  {
+    const long long lim = (long long)K << 14;
+    int bits = 0;
+    while ((1ll << bits) <= lim) ++bits;
+    const int f = bits + 1, count_bits = 64 - 2 * f;
+    const GemmSplit sp = make_gemm_split(pl.n_tiles, pl.kb, pl.blocks);
+    int most = 0;
+    for (int t = 0; t < pl.n_tiles; ++t) {
+      const int c = gemm_split_contributors(sp, t);
+      most = c > most ? c : most;
+    }
+    pl.pack_f = (count_bits >= 1 && count_bits < 63 && (long long)most < (1ll << count_bits)) ? f : 0;
   }
   pl.threads = kThreads;
   pl.stage_slabs = kStageSlabs;
@@ -531,6 +608,7 @@ cudaError_t gemm_launch(const GemmPlan& pl, const int8_t* x, const float* xs, co
   p.N = N;
   p.KB = pl.kb;
   p.split = make_gemm_split(pl.n_tiles, pl.kb, pl.blocks);
+  p.pack_f = pl.pack_f;
   p.pdl = pdl ? 1 : 0;
   switch (pl.nt8) {
     case 1: return launch_gemm<1, kStages1>(p, pl.blocks, pdl, stream);

@@ -124,6 +124,48 @@ def test_plan_shape_and_limits():
     assert all(lib8.w8a8_plan(M, 4096, 1536)["workspace_bytes"] <= big for M in range(1, 33))
 
 
+def test_two_element_combine_words():
+    # Field width from K (partial sums of an element are at most K * 2^14 in magnitude) and the
+    # arrival count in the remaining bits; one element per word when the count would not fit.
+    assert lib8.w8a8_plan(16, 4096, 1536)["combine_pack_bits"] == 28
+    assert lib8.w8a8_plan(16, 12288, 4096)["combine_pack_bits"] == 29
+    assert lib8.w8a8_plan(16, 4096, 1536, 3072)["combine_pack_bits"] == 28      # 128 CTAs per tile
+    assert lib8.w8a8_plan(32, 12288, 128)["combine_pack_bits"] == 0             # 152 > 63 per tile
+    assert lib8.w8a8_plan(1, 65536, 64, 1)["combine_pack_bits"] == 0            # fields too wide
+
+
+def test_two_element_word_arithmetic():
+    # Host emulation of the combine word: every CTA adds 2^(2f) + b * 2^f + a (mod 2^64) and
+    # decodes the sums and count of the partials added before its own from the returned word.
+    rng = np.random.default_rng(5)
+    M64 = (1 << 64) - 1
+    def sext(v, f):
+        v &= (1 << f) - 1
+        return v - (1 << f) if v >> (f - 1) else v
+    for K, n in ((4096, 13), (4096, 255), (12288, 63), (32, 1000)):
+        f = (K << 14).bit_length() + 1
+        assert 64 - 2 * f >= 1 and n < 1 << (64 - 2 * f)
+        lim = K << 14
+        for trial in range(20):
+            # partials of n CTAs over disjoint k-ranges: their sum stays within +-K * 2^14
+            cuts = np.sort(rng.choice(np.arange(1, K), size=min(n - 1, K - 1), replace=False)) if n > 1 else []
+            ks = np.diff(np.concatenate([[0], cuts, [K]])).astype(np.int64)
+            extreme = trial % 3
+            pa = [int(k) * (16384 if extreme == 0 else -16256 if extreme == 1 else int(rng.integers(-16384, 16385)))
+                  for k in ks]
+            pb = [int(k) * int(rng.integers(-16384, 16385)) for k in ks]
+            w = 0
+            for i, (a, b) in enumerate(zip(pa, pb)):
+                old = w
+                a_old = sext(old, f)
+                w1 = ((old - a_old) & M64) >> f
+                b_old = sext(w1, f)
+                cnt = ((w1 - b_old) & M64) >> f
+                assert (a_old, b_old, cnt) == (sum(pa[:i]), sum(pb[:i]), i)
+                w = (old + (1 << (2 * f)) + (b << f) + a) & M64
+            assert abs(sum(pa)) <= lim and abs(sum(pb)) <= lim
+
+
 @pytest.mark.parametrize("M,K,N,blocks,code", [
     (0, 512, 256, 0, 1), (33, 512, 256, 0, 1), (1, 0, 256, 0, 1), (1, 512, 0, 0, 1),
     (1, 500, 256, 0, 2), (1, 512, 250, 0, 2), (1, 512, 256, -1, 1), (1, 512, 256, 10**6, 1)])

@@ -233,3 +233,21 @@ def test_pdl_graph_replay_chain():
         for (_, ref), o in zip(cases, outs):
             np.testing.assert_array_equal(bf16_bits(o), ref)
     del out
+
+
+@pytest.mark.parametrize("fx,fw", [(-128, -128), (127, -128), (-128, 127)])
+def test_two_element_combine_at_its_range_limits(fx, fw):
+    # K = 4096 with constant extremes drives every element's partial sums to the edge of the
+    # two-element word's fields (|sum| up to K * 2^14 = 2^26 in 28-bit fields), with 128 CTAs per
+    # tile (the count field's 8 bits near full).
+    M, K, N = 32, 4096, 128
+    x = np.full((M, K), fx, np.int8)
+    W = np.full((K, N), fw, np.int8)
+    x[5] = -x[5] if fx != -128 else 127
+    xs = np.full(M, 2.0**-12, np.float32)
+    ws = np.full(N, 2.0**-14, np.float32)
+    for blocks in (256, 0, 5):
+        case = W8A8Case(x, xs, W, ws, blocks=blocks)
+        if blocks == 256:
+            assert lib8.w8a8_plan(M, K, N, blocks)["combine_pack_bits"] == 28
+        _check(case, x, xs, W, ws)
