@@ -367,6 +367,18 @@ def run_ours(args):
         "e2e": {k: (round(v, 3) if isinstance(v, float) else v) for k, v in res["e2e"].items()},
         "clocks": res["clocks"],
     }
+    # The same calls launched with programmatic dependent launch (W8A8_FLAG_PDL): each call starts
+    # streaming its weight while the previous call finishes, as in a chain of decode-step GEMMs.
+    # Reported beside the default line, not as its value.
+    import int8_weight_gemm_gb300 as lib8
+    rp = time_gemm(M, K, N, cfg["dist"], cfg["seed"], min(args.steps, 300), args.warmup, device=dev,
+                   want_e2e=False, flags=lib8.W8A8_FLAG_PDL)
+    rp.pop("inputs")
+    out["pdl"] = {"value": round(world * wbytes * rp["launches"] / (rp["total_ms"] / 1e3) / 1e9, 2), "unit": "GB/s",
+                  "us_per_call": {"median": round(rp["us_median"], 4), "p90": round(rp["us_p90"], 4)},
+                  "roofline_frac": round(alg_bytes / (rp["avg_launch_us"] * 1e-6) / 1e9 / peak, 4),
+                  "launch": "W8A8_FLAG_PDL, same graph of rotating-weight calls"}
+    del rp
     # one-call correctness check of the timed configuration against the oracle (first 4 rows)
     if rank == 0:
         import oracle
