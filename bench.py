@@ -387,7 +387,8 @@ def run_ours(args):
         out["parity_rows_checked"] = int(4)
         out["parity_mismatches"] = int(np.count_nonzero(got != ref))
         if not args.no_q8:
-            out["q8_0"] = [time_q8(T, K8, N8) for (K8, N8) in ((4096, 320), (320, 4096)) for T in (1, 4, 6)]
+            out["q8_0"] = [time_q8(T, K8, N8, flags=f) for (K8, N8) in ((4096, 320), (320, 4096)) for T in (1, 4, 6)
+                           for f in (0, lib8.W8A8_FLAG_PDL)]
         if not args.no_cpu:
             out["cpu_baseline"] = cpu_baseline(M, K, N, x, xs, W, ws)
     if world > 1:

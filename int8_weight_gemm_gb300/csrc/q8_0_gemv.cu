@@ -19,9 +19,12 @@
 
 namespace w8a8 {
 
-constexpr int kQ8MaxWarps = 4;
+constexpr int kQ8MaxWarps = 16;
 constexpr int kQ8MaxBlocksPerWarp = 8;
 constexpr int kQ8TargetBlocksPerWarp = 4;
+// One CTA covers up to 16 warps x 8 blocks = 4096 k of a tile, so K <= 4096 needs no cross-CTA
+// combine: its two dependent global round trips (counter, then the partials) cost more than the
+// extra loads each warp keeps in flight.
 
 struct Q8Params {
   const uint16_t* x;
@@ -198,10 +201,11 @@ int q8_plan(int T, int K, int N, Q8Plan* plan) {
   Q8Plan pl{};
   pl.n_tiles = (N + 15) / 16;
   pl.kb = K / 32;
-  int warps = (pl.kb + kQ8TargetBlocksPerWarp - 1) / kQ8TargetBlocksPerWarp;
-  pl.warps = warps < kQ8MaxWarps ? warps : kQ8MaxWarps;
-  const int per_cta = pl.warps * kQ8TargetBlocksPerWarp;
-  pl.splits = (pl.kb + per_cta - 1) / per_cta;
+  const int per_cta_max = kQ8MaxWarps * kQ8MaxBlocksPerWarp;
+  pl.splits = (pl.kb + per_cta_max - 1) / per_cta_max;
+  const int per_split = (pl.kb + pl.splits - 1) / pl.splits;
+  const int warps = (per_split + kQ8TargetBlocksPerWarp - 1) / kQ8TargetBlocksPerWarp;
+  pl.warps = warps < kQ8MaxWarps ? warps : kQ8MaxWarps;   // then at most 8 blocks per warp
   pl.blocks = pl.n_tiles * pl.splits;
   const size_t counters = ((size_t)pl.n_tiles * 4 + 255) / 256 * 256;
   const size_t partials = pl.splits > 1 ? (size_t)pl.n_tiles * pl.splits * 32 * 16 : 0;
