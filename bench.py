@@ -271,6 +271,31 @@ def time_e2e(lib8, M, K, N, xd, xsd, packs, wsd, wsp, blocks, dev, steps, flags=
             "h2d_bytes_per_step": M * K + 4 * M, "d2h_bytes_per_step": 2 * M * N}
 
 
+def time_read_ceiling(dev, nbytes=1 << 30, reps=20):
+    """The library's read-only probe over a buffer much larger than L2: the achievable HBM read rate."""
+    import torch
+
+    import int8_weight_gemm_gb300 as lib8
+
+    buf = torch.randint(0, 256, (nbytes,), dtype=torch.uint8, device=dev)
+    sink = torch.zeros(1, dtype=torch.int64, device=dev)
+    for _ in range(3):
+        lib8.w8a8_read_probe(buf, sink)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        lib8.w8a8_read_probe(buf, sink)
+    e1.record()
+    torch.cuda.synchronize(dev)
+    s = e0.elapsed_time(e1) / 1e3
+    del buf
+    torch.cuda.empty_cache()
+    return {"value": round(nbytes * reps / s / 1e9, 1), "unit": "GB/s", "bytes_per_read": nbytes,
+            "kernel": "w8a8_read_probe (16-byte loads, 2 x SMs x 512 threads)"}
+
+
 def time_q8(T, K, N, iters=200, seed=7, flags=0):
     """Median us per Q8_0 read in a graph of calls over rotating weight sets (not L2-resident)."""
     import torch
@@ -389,6 +414,8 @@ def run_ours(args):
         if not args.no_q8:
             out["q8_0"] = [time_q8(T, K8, N8, flags=f) for (K8, N8) in ((4096, 320), (320, 4096)) for T in (1, 4, 6)
                            for f in (0, lib8.W8A8_FLAG_PDL)]
+        out["read_ceiling"] = time_read_ceiling(dev)
+        out["roofline"]["frac_of_read_ceiling"] = round(achieved / out["read_ceiling"]["value"], 4)
         if not args.no_cpu:
             out["cpu_baseline"] = cpu_baseline(M, K, N, x, xs, W, ws)
     if world > 1:

@@ -196,6 +196,14 @@ int w8a8_gemm_no_alloc(const int8_t* x_q, const float* x_scale, const void* W_pa
  * ----------------------------------------------------------------------------------------- */
 
 /* Workspace bytes that q8_0_gemv needs for every T in [1, T_max] at (K, N). */
+/* Measurement helper (not part of either operator): reads `bytes` (rounded down to a multiple of
+ * 16) of device memory at `buf` once with 16-byte vector loads, on 2 x SM-count CTAs of 512
+ * threads, and discards the data (a 64-bit device word at `sink` is written only in a case that
+ * real data practically never produce).  Timed over a buffer larger than L2 it gives the
+ * achievable HBM read rate, the ceiling for the weight stream.  buf 16-byte aligned, sink 8-byte
+ * aligned.  Errors: INVALID_ARG, MISALIGNED, CUDA. */
+int w8a8_read_probe(const void* buf, size_t bytes, void* sink, void* stream);
+
 size_t q8_0_workspace_bytes(int T_max, int K, int N);
 
 /* y[t][n] = bf16_rne( sum_k x[t][k] * (d[n][k/32] * q[n][k]) ), summed in fp32 in a fixed order

@@ -26,6 +26,7 @@ __all__ = [
     "q8_0_gemv",
     "w8a8_plan",
     "w8a8_split_bounds",
+    "w8a8_read_probe",
     "alloc_workspace",
 ]
 
@@ -70,6 +71,7 @@ SIGNATURES = {
     "w8a8_plan": ([_c_i, _c_i, _c_i, _c_i, ctypes.POINTER(PlanT)], _c_i),
     "w8a8_split_bounds": ([_c_i, _c_i, _c_i, ctypes.POINTER(ctypes.c_longlong), _c_i], _c_i),
     "q8_0_workspace_bytes": ([_c_i, _c_i, _c_i], _c_sz),
+    "w8a8_read_probe": ([_c_p, _c_sz, _c_p, _c_p], _c_i),
     "q8_0_gemv": ([_c_p, _c_p, _c_p, _c_p, _c_i, _c_i, _c_i, ctypes.c_uint, _c_p, _c_sz, _c_p], _c_i),
 }
 
@@ -218,3 +220,9 @@ def q8_0_gemv(x, q, d, ws, y=None, flags: int = 0, stream=None):
                          _stream(stream))
     _check("q8_0_gemv", rc)
     return y
+
+
+def w8a8_read_probe(buf, sink, stream=None) -> None:
+    """Read the whole device tensor `buf` once (16-byte loads) and discard it: the HBM read-rate
+    probe.  `sink` is an 8-byte device tensor the kernel may write."""
+    _check("w8a8_read_probe", lib().w8a8_read_probe(_ptr(buf), _nbytes(buf), _ptr(sink), _stream(stream)))

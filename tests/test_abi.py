@@ -175,6 +175,15 @@ def test_plan_rejects_bad_shapes(M, K, N, blocks, code):
     assert lib8.w8a8_workspace_bytes(M, K, N, blocks) == 0 or code == 0
 
 
+def test_read_probe_checks_its_arguments_on_the_host():
+    L = lib8.lib()
+    a = ctypes.c_void_p(1 << 20)
+    assert L.w8a8_read_probe(None, 1 << 20, a, None) == 1
+    assert L.w8a8_read_probe(a, 8, a, None) == 1
+    assert L.w8a8_read_probe(ctypes.c_void_p((1 << 20) + 8), 1 << 20, a, None) == 3
+    assert L.w8a8_read_probe(a, 1 << 20, ctypes.c_void_p((1 << 20) + 4), None) == 3
+
+
 def test_calls_with_null_pointers_fail_before_any_launch():
     L = lib8.lib()
     null = ctypes.c_void_p(0)

@@ -251,3 +251,12 @@ def test_two_element_combine_at_its_range_limits(fx, fw):
         if blocks == 256:
             assert lib8.w8a8_plan(M, K, N, blocks)["combine_pack_bits"] == 28
         _check(case, x, xs, W, ws)
+
+
+def test_read_probe_runs_and_leaves_its_input_alone():
+    buf = torch.randint(0, 256, (1 << 22,), dtype=torch.uint8, device="cuda")
+    ref = buf.clone()
+    sink = torch.zeros(1, dtype=torch.int64, device="cuda")
+    lib8.w8a8_read_probe(buf, sink)
+    torch.cuda.synchronize()
+    assert torch.equal(buf, ref)
