@@ -53,6 +53,14 @@ def lib():
         L.oracle_w8a8_packed_bytes.restype = ctypes.c_size_t
         L.oracle_w8a8_pack.argtypes = [c_p, c_i, c_i, c_p]
         L.oracle_w8a8_pack.restype = None
+        L.oracle_f16_from_f32.argtypes = [ctypes.c_float]
+        L.oracle_f16_from_f32.restype = ctypes.c_uint16
+        L.oracle_q8_0_quantize.argtypes = [c_p, c_i, c_i, c_p, c_p]
+        L.oracle_q8_0_quantize.restype = None
+        L.oracle_w8a8_quantize_rows.argtypes = [c_p, c_i, c_i, c_p, c_p]
+        L.oracle_w8a8_quantize_rows.restype = None
+        L.oracle_q8_0_blocks_from_split.argtypes = [c_p, c_p, c_i, c_i, c_p]
+        L.oracle_q8_0_blocks_from_split.restype = None
         _lib = L
     return _lib
 
@@ -197,3 +205,42 @@ def q8_0_split_from_blocks(blocks: np.ndarray, K: int, N: int):
     d = np.zeros((N, K // 32), dtype=np.uint16)
     lib().oracle_q8_0_split_from_blocks(_ptr(blocks), K, N, _ptr(q), _ptr(d))
     return q, d
+
+
+def f16_from_f32(values) -> np.ndarray:
+    """float32 values -> IEEE half bit patterns, round to nearest even (oracle.c)."""
+    v = np.asarray(values, dtype=np.float32).ravel()
+    L = lib()
+    return np.array([L.oracle_f16_from_f32(float(f)) for f in v], dtype=np.uint16).reshape(np.shape(values))
+
+
+def q8_0_quantize(w_bits: np.ndarray):
+    """BF16 weights [N, K] (uint16 bits) -> (q [N, K] int8, d [N, K/32] fp16 bits), ggml's
+    rounding as the Q8_0 page states it (oracle.c: oracle_q8_0_quantize)."""
+    w = _c(w_bits, np.uint16)
+    N, K = w.shape
+    q = np.empty((N, K), dtype=np.int8)
+    d = np.empty((N, K // 32), dtype=np.uint16)
+    lib().oracle_q8_0_quantize(_ptr(w), K, N, _ptr(q), _ptr(d))
+    return q, d
+
+
+def w8a8_quantize_rows(x_bits: np.ndarray):
+    """BF16 activations [M, K] (uint16 bits) -> (x_q [M, K] int8, x_scale [M] float32), one
+    symmetric scale per row (oracle.c: oracle_w8a8_quantize_rows)."""
+    x = _c(x_bits, np.uint16)
+    M, K = x.shape
+    xq = np.empty((M, K), dtype=np.int8)
+    xs = np.empty(M, dtype=np.float32)
+    lib().oracle_w8a8_quantize_rows(_ptr(x), M, K, _ptr(xq), _ptr(xs))
+    return xq, xs
+
+
+def q8_0_blocks_from_split(q: np.ndarray, d_bits: np.ndarray) -> np.ndarray:
+    """Split layout -> ggml-style 34-byte blocks [N, K/32, 34] (oracle.c)."""
+    qc = _c(q, np.int8)
+    dc = _c(d_bits, np.uint16)
+    N, K = qc.shape
+    out = np.empty((N, K // 32, 34), dtype=np.uint8)
+    lib().oracle_q8_0_blocks_from_split(_ptr(qc), _ptr(dc), K, N, _ptr(out))
+    return out

@@ -237,3 +237,104 @@ void oracle_w8a8_pack(const int8_t* W, int K, int N, uint8_t* packed) {
                         packed[off] = n < N ? (uint8_t)(((uint8_t)W[(size_t)k * N + n]) ^ 0x80u) : 0x80u;
                     }
 }
+
+/* ---------------------------------------------------------------------------------------
+ * Load-time and input-side quantisation (the rows after the hot path).
+ * ------------------------------------------------------------------------------------- */
+
+/* bfloat16 bits -> float32: the bfloat16 encoding is the top half of the float32 one. */
+static float bf16_to_f32(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* float32 -> IEEE half bits, round to nearest, ties to even, from the two encodings.  A half
+ * has 10 stored mantissa bits and exponent bias 15: normal halves cover [2^-14, 65504], the
+ * subnormals are multiples of 2^-24 below 2^-14, and magnitudes from 65520 (halfway between
+ * 65504 and 2^16) round to infinity. */
+uint16_t oracle_f16_from_f32(float f) {
+    uint32_t x;
+    memcpy(&x, &f, 4);
+    const uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+    const uint32_t ax = x & 0x7FFFFFFFu;
+    if (ax > 0x7F800000u) return (uint16_t)(sign | 0x7E00u);   /* NaN */
+    if (ax >= 0x477FF000u) return (uint16_t)(sign | 0x7C00u);  /* >= 65520: infinity */
+    if (ax < 0x38800000u) {                                   /* below 2^-14: subnormal or zero */
+        const uint32_t e = ax >> 23;
+        if (e < 102) return sign;                              /* below 2^-25 (ties at 2^-25 go to 0) */
+        const uint32_t m = (ax & 0x7FFFFFu) | 0x800000u;       /* value = m * 2^(e - 150) */
+        const uint32_t shift = 126 - e;                        /* in units of 2^-24: m >> shift */
+        uint32_t r = m >> shift;
+        const uint32_t rem = m & ((1u << shift) - 1u), half = 1u << (shift - 1u);
+        if (rem > half || (rem == half && (r & 1u))) ++r;
+        return (uint16_t)(sign | r);
+    }
+    const uint32_t rebased = ax - 0x38000000u;                 /* exponent bias 127 -> 15 */
+    uint32_t r = rebased >> 13;
+    const uint32_t rem = rebased & 0x1FFFu;
+    if (rem > 0x1000u || (rem == 0x1000u && (r & 1u))) ++r;    /* a carry moves into the exponent */
+    return (uint16_t)(sign | r);
+}
+
+/* Q8_0 quantisation of BF16 weights at load.  [Q8_0] "What changed", the loader bullet: a BF16
+ * tensor is quantised on the host with ggml's rounding, d = amax / 127 stored as fp16 and
+ * q = round(x / d), then uploaded in the split layout.  Readings where the pages are silent:
+ * amax is taken over the 32 values of a block (the block is Q8_0's unit); the d that divides x
+ * is the float32 quotient amax / 127, before it is stored as fp16; round is C's roundf (halves
+ * away from zero); a block whose amax is 0 gets d = 0 and q = 0.
+ *   w [N, K] bf16 bits, row-major -> q [N, K] int8, d [N, K / 32] fp16 bits. */
+void oracle_q8_0_quantize(const uint16_t* w, int K, int N, int8_t* q, uint16_t* d) {
+    const int nb = K / 32;
+    for (int n = 0; n < N; ++n) {
+        for (int b = 0; b < nb; ++b) {
+            const uint16_t* blk = w + (size_t)n * K + (size_t)b * 32;
+            float amax = 0.0f;
+            for (int j = 0; j < 32; ++j) {
+                const float a = fabsf(bf16_to_f32(blk[j]));
+                if (a > amax) amax = a;
+            }
+            const float dd = amax / 127.0f;
+            d[(size_t)n * nb + b] = oracle_f16_from_f32(dd);
+            for (int j = 0; j < 32; ++j)
+                q[(size_t)n * K + (size_t)b * 32 + j] = dd == 0.0f ? 0 : (int8_t)roundf(bf16_to_f32(blk[j]) / dd);
+        }
+    }
+}
+
+/* Per-row symmetric int8 quantisation of bf16 activations, the input side of the W8A8 operator.
+ * [W8A8] operator line: x_q[M,K] int8 with x_scale[M,1], and the timed region "excludes
+ * quantization" - the pages fix the scale's shape but not how it is computed.  Reading: the
+ * Q8_0 loader's convention with one block per row, x_scale[m] = amax_m / 127 (float32) and
+ * x_q[m][k] = roundf(x[m][k] / x_scale[m]), 0 for a row whose amax is 0.
+ *   x [M, K] bf16 bits, row-major -> x_q [M, K] int8, x_scale [M] float32. */
+void oracle_w8a8_quantize_rows(const uint16_t* x, int M, int K, int8_t* x_q, float* x_scale) {
+    for (int m = 0; m < M; ++m) {
+        const uint16_t* row = x + (size_t)m * K;
+        float amax = 0.0f;
+        for (int k = 0; k < K; ++k) {
+            const float a = fabsf(bf16_to_f32(row[k]));
+            if (a > amax) amax = a;
+        }
+        const float s = amax / 127.0f;
+        x_scale[m] = s;
+        for (int k = 0; k < K; ++k)
+            x_q[(size_t)m * K + k] = s == 0.0f ? 0 : (int8_t)roundf(bf16_to_f32(row[k]) / s);
+    }
+}
+
+/* The split layout -> ggml-style interleaved blocks (the inverse of oracle_q8_0_split_from_blocks):
+ * per block the fp16 scale (little-endian), then its 32 quants; 34 bytes. */
+void oracle_q8_0_blocks_from_split(const int8_t* q, const uint16_t* d, int K, int N, uint8_t* blocks) {
+    const int nb = K / 32;
+    for (int n = 0; n < N; ++n) {
+        for (int b = 0; b < nb; ++b) {
+            uint8_t* blk = blocks + ((size_t)n * nb + b) * 34;
+            const uint16_t s = d[(size_t)n * nb + b];
+            blk[0] = (uint8_t)(s & 0xFFu);
+            blk[1] = (uint8_t)(s >> 8);
+            for (int j = 0; j < 32; ++j) blk[2 + j] = (uint8_t)q[(size_t)n * K + (size_t)b * 32 + j];
+        }
+    }
+}

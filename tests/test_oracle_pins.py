@@ -334,3 +334,99 @@ def test_pack_places_each_weight_once():
             # the stored cell lies in the 64-row tile of n and the 32-wide k block of k
             t, kb = hit[0] // (K // 32 * 2048), (hit[0] // 2048) % (K // 32)
             assert t == n // 64 and kb == k // 32
+
+
+# --------------------------------------------------------------------------------------------
+# Quantisation rows (activation quantisation in front of W8A8; Q8_0 from BF16 at load)
+# --------------------------------------------------------------------------------------------
+
+def _bf16_bits(values):
+    """float values exactly representable in bf16 -> their bf16 bit patterns (via torch)."""
+    t = torch.tensor(np.asarray(values, dtype=np.float32)).to(torch.bfloat16)
+    assert torch.equal(t.float(), torch.tensor(np.asarray(values, dtype=np.float32)))   # exact
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def test_f16_from_f32_matches_numpy():
+    # Edges: largest half, the first value that rounds to infinity, subnormals, halfway cases
+    # (low 13 bits exactly 0x1000, both parities), and random values over every exponent.
+    edge = [0.0, -0.0, 1.0, -1.0, 65504.0, 65519.99, 65520.0, 2.0**-14, 2.0**-24, 2.0**-25, 3 * 2.0**-25,
+            2.0**-25 * 1.0001, 1.0 + 2.0**-11, 1.0 + 3 * 2.0**-11, 1.0 + 2.0**-11 + 2.0**-20, 1e-3, 1e-2, 0.1]
+    rng = np.random.default_rng(3)
+    rand = (rng.standard_normal(20000) * np.exp2(rng.integers(-30, 17, 20000))).astype(np.float32)
+    vals = np.concatenate([np.array(edge, np.float32), rand])
+    with np.errstate(over="ignore"):
+        ref = vals.astype(np.float16).view(np.uint16)
+    np.testing.assert_array_equal(oracle.f16_from_f32(vals), ref)
+
+
+def test_q8_0_quantize_exact_multiples_and_ties():
+    # d = (127 / 8) / 127 = 1/8 exactly (fp16 0x3000).  Row 0: x = k/8 gives q = k.  Row 1:
+    # x = (n + 1/2)/8 is a tie, rounded away from zero (ggml's roundf), not to even.  Row 2: a zero
+    # block gives d = 0, q = 0.  Row 3: the amax element is negative and maps to -127.
+    K = 32
+    k = np.array(list(range(-15, 16)) + [127], dtype=np.float64)
+    ties = np.array([0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 126.5, -126.5] + [0.0] * 23 + [127.0])
+    rows = np.stack([k / 8, ties / 8, np.zeros(K), np.array([-127.0] + [3.0] * 31) / 8])
+    q, d = oracle.q8_0_quantize(_bf16_bits(rows))
+    assert d.tolist() == [[0x3000], [0x3000], [0], [0x3000]]
+    np.testing.assert_array_equal(q[0], k.astype(np.int8))
+    np.testing.assert_array_equal(q[1, :8], [1, 2, 3, -1, -2, -3, 127, -127])
+    assert q[1, -1] == 127 and (q[2] == 0).all()
+    assert q[3, 0] == -127 and (q[3, 1:] == 3).all()         # (3/8) / (1/8) = 3
+
+
+def test_q8_0_quantize_invariants_random():
+    # Random bf16 weights: |x - q d| <= d / 2 (rounding to the nearest integer, d the float32
+    # amax / 127), |q| <= 127 with the amax element at +-127, and the stored scale is numpy's
+    # float16 of that float32 quotient.
+    rng = np.random.default_rng(11)
+    N, K = 24, 256
+    w = torch.tensor(rng.standard_normal((N, K)).astype(np.float32) * 0.02).to(torch.bfloat16)
+    wb = w.view(torch.int16).numpy().view(np.uint16)
+    wf = w.float().numpy().reshape(N, K // 32, 32)
+    q, d = oracle.q8_0_quantize(wb)
+    amax = np.abs(wf).max(axis=2).astype(np.float32)
+    d32 = amax / np.float32(127)
+    np.testing.assert_array_equal(d, d32.astype(np.float16).view(np.uint16))
+    qb = q.reshape(N, K // 32, 32).astype(np.float64)
+    err = np.abs(wf.astype(np.float64) - qb * d32[..., None].astype(np.float64))
+    assert (err <= d32[..., None] * (0.5 + 2.0**-16)).all()      # x / d rounds once in fp32 (|x / d| <= 127)
+    assert np.abs(q).max() <= 127
+    at = np.argmax(np.abs(wf), axis=2)
+    np.testing.assert_array_equal(np.abs(np.take_along_axis(qb, at[..., None], axis=2)[..., 0]), 127)
+
+
+def test_w8a8_quantize_rows_closed_forms_and_invariants():
+    # Row-wise: same closed forms as a Q8_0 block spanning the whole row, plus random rows.
+    K = 64
+    r0 = np.array(list(range(-31, 32)) + [127], dtype=np.float64) / 4           # scale 1/4: q = 4x
+    r1 = np.zeros(K)
+    r2 = np.array([2.5, -2.5, 0.5] + [0.0] * 60 + [-127.0]) / 4                 # ties away from zero
+    xq, xs = oracle.w8a8_quantize_rows(_bf16_bits(np.stack([r0, r1, r2])))
+    assert xs.tolist() == [0.25, 0.0, 0.25]
+    np.testing.assert_array_equal(xq[0], (r0 * 4).astype(np.int8))
+    assert (xq[1] == 0).all()
+    assert xq[2, :3].tolist() == [3, -3, 1] and xq[2, -1] == -127
+    rng = np.random.default_rng(12)
+    x = torch.tensor(rng.standard_normal((16, 4096)).astype(np.float32)).to(torch.bfloat16)
+    xq, xs = oracle.w8a8_quantize_rows(x.view(torch.int16).numpy().view(np.uint16))
+    xf = x.float().numpy().astype(np.float64)
+    np.testing.assert_array_equal(xs, (np.abs(x.float().numpy()).max(axis=1) / np.float32(127)).astype(np.float32))
+    assert (np.abs(xf - xq * xs[:, None].astype(np.float64)) <= xs[:, None] * (0.5 + 2.0**-16)).all()
+    assert (np.abs(xq).max(axis=1) == 127).all()
+
+
+def test_q8_0_blocks_and_split_layout_are_inverse():
+    rng = np.random.default_rng(13)
+    N, K = 5, 96
+    q = rng.integers(-128, 128, (N, K)).astype(np.int8)
+    d = rng.integers(0, 1 << 16, (N, K // 32)).astype(np.uint16)
+    blocks = oracle.q8_0_blocks_from_split(q, d)
+    assert blocks.shape == (N, K // 32, 34)
+    # byte-level check of one block from the definition: little-endian scale, then the 32 quants
+    assert blocks[2, 1, 0] == d[2, 1] & 0xFF and blocks[2, 1, 1] == d[2, 1] >> 8
+    np.testing.assert_array_equal(blocks[2, 1, 2:].view(np.int8), q[2, 32:64])
+    q2, d2 = oracle.q8_0_split_from_blocks(blocks, K, N)
+    np.testing.assert_array_equal(q2, q)
+    np.testing.assert_array_equal(d2, d)
