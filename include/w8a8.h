@@ -196,6 +196,36 @@ int w8a8_gemm_no_alloc(const int8_t* x_q, const float* x_scale, const void* W_pa
  * ----------------------------------------------------------------------------------------- */
 
 /* Workspace bytes that q8_0_gemv needs for every T in [1, T_max] at (K, N). */
+/* ---------------------------------------------------------------------------------------------
+ * Quantisation around the operators (outside the timed GEMM / read).  Sources: the Q8_0 page
+ * ("sycl: STRATA_HC_Q8=1 reads the Q8_0 hyper-connection projections", section "What changed",
+ * the loader bullet: d = amax / 127 stored as fp16, q = round(x / d), split layout); the W8A8
+ * page's operator line (x_q int8 with x_scale[M,1]; quantisation is outside the timed region).
+ * Readings: amax per 32-value block (Q8_0) or per row (activations); x is divided by the float32
+ * scale; round = C roundf (halves away from zero); an all-zero block or row gets scale 0 and
+ * quants 0; inputs are finite.  Division and fp16 conversion round to nearest even, so results
+ * are bit-identical to a scalar IEEE evaluation.  All pointers are device pointers; each call is
+ * one kernel launch on `stream`, graph-capture safe, with every check done before it.
+ * ------------------------------------------------------------------------------------------- */
+
+/* x [M,K] bf16 row-major (16-byte aligned) -> x_q [M,K] int8 (8-byte aligned) and
+ * x_scale [M] fp32: x_scale[m] = max_k |x[m][k]| / 127, x_q[m][k] = roundf(x[m][k] / x_scale[m]).
+ * 1 <= M <= 2^20, 8 <= K <= 65536, K % 8 == 0.  Errors: INVALID_ARG, UNSUPPORTED_SHAPE,
+ * MISALIGNED, CUDA. */
+int w8a8_quantize_activations(const void* x, int8_t* x_q, float* x_scale, int M, int K, void* stream);
+
+/* Q8_0 from BF16 weights: w [N,K] bf16 row-major (16-byte aligned) -> the split layout of
+ * q8_0_gemv, q [N,K] int8 (8-byte aligned) and d [N,K/32] fp16 (2-byte aligned), per block of 32
+ * along K: d = fp16_rn(amax / 127), q = roundf(w / (amax / 127)).  K % 32 == 0, 32 <= K <= 65536,
+ * 1 <= N <= 2^20.  Errors as above. */
+int q8_0_quantize(const void* w, int8_t* q, void* d, int K, int N, void* stream);
+
+/* ggml-style Q8_0 rows (per block: the fp16 scale little-endian, then its 32 quants; 34 bytes;
+ * blocks [N][K/32], 2-byte aligned) -> the split layout (q [N,K] 16-byte aligned, d [N,K/32]), and
+ * back.  The same bytes, reordered.  Limits and errors as for q8_0_quantize. */
+int q8_0_split_from_blocks(const void* blocks, int8_t* q, void* d, int K, int N, void* stream);
+int q8_0_blocks_from_split(const int8_t* q, const void* d, void* blocks, int K, int N, void* stream);
+
 /* Measurement helper (not part of either operator): reads `bytes` (rounded down to a multiple of
  * 16) of device memory at `buf` once with 16-byte vector loads, on 2 x SM-count CTAs of 512
  * threads, and discards the data (a 64-bit device word at `sink` is written only in a case that

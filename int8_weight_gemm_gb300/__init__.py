@@ -27,6 +27,10 @@ __all__ = [
     "w8a8_plan",
     "w8a8_split_bounds",
     "w8a8_read_probe",
+    "w8a8_quantize_activations",
+    "q8_0_quantize",
+    "q8_0_split_from_blocks",
+    "q8_0_blocks_from_split",
     "alloc_workspace",
 ]
 
@@ -72,6 +76,10 @@ SIGNATURES = {
     "w8a8_split_bounds": ([_c_i, _c_i, _c_i, ctypes.POINTER(ctypes.c_longlong), _c_i], _c_i),
     "q8_0_workspace_bytes": ([_c_i, _c_i, _c_i], _c_sz),
     "w8a8_read_probe": ([_c_p, _c_sz, _c_p, _c_p], _c_i),
+    "w8a8_quantize_activations": ([_c_p, _c_p, _c_p, _c_i, _c_i, _c_p], _c_i),
+    "q8_0_quantize": ([_c_p, _c_p, _c_p, _c_i, _c_i, _c_p], _c_i),
+    "q8_0_split_from_blocks": ([_c_p, _c_p, _c_p, _c_i, _c_i, _c_p], _c_i),
+    "q8_0_blocks_from_split": ([_c_p, _c_p, _c_p, _c_i, _c_i, _c_p], _c_i),
     "q8_0_gemv": ([_c_p, _c_p, _c_p, _c_p, _c_i, _c_i, _c_i, ctypes.c_uint, _c_p, _c_sz, _c_p], _c_i),
 }
 
@@ -226,3 +234,53 @@ def w8a8_read_probe(buf, sink, stream=None) -> None:
     """Read the whole device tensor `buf` once (16-byte loads) and discard it: the HBM read-rate
     probe.  `sink` is an 8-byte device tensor the kernel may write."""
     _check("w8a8_read_probe", lib().w8a8_read_probe(_ptr(buf), _nbytes(buf), _ptr(sink), _stream(stream)))
+
+
+def w8a8_quantize_activations(x, x_q=None, x_scale=None, stream=None):
+    """bf16 x [M, K] -> (x_q [M, K] int8, x_scale [M] fp32), one symmetric scale per row."""
+    import torch
+
+    M, K = x.shape
+    if x_q is None:
+        x_q = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    if x_scale is None:
+        x_scale = torch.empty(M, dtype=torch.float32, device=x.device)
+    _check("w8a8_quantize_activations",
+           lib().w8a8_quantize_activations(_ptr(x), _ptr(x_q), _ptr(x_scale), M, K, _stream(stream)))
+    return x_q, x_scale
+
+
+def q8_0_quantize(w, q=None, d=None, stream=None):
+    """bf16 weights w [N, K] -> Q8_0 split layout (q [N, K] int8, d [N, K/32] fp16 bits as int16)."""
+    import torch
+
+    N, K = w.shape
+    if q is None:
+        q = torch.empty((N, K), dtype=torch.int8, device=w.device)
+    if d is None:
+        d = torch.empty((N, K // 32), dtype=torch.int16, device=w.device)
+    _check("q8_0_quantize", lib().q8_0_quantize(_ptr(w), _ptr(q), _ptr(d), K, N, _stream(stream)))
+    return q, d
+
+
+def q8_0_split_from_blocks(blocks, K: int, N: int, q=None, d=None, stream=None):
+    """ggml Q8_0 blocks (uint8, N * K/32 * 34 bytes) -> (q [N, K] int8, d [N, K/32] int16 bits)."""
+    import torch
+
+    if q is None:
+        q = torch.empty((N, K), dtype=torch.int8, device=blocks.device)
+    if d is None:
+        d = torch.empty((N, K // 32), dtype=torch.int16, device=blocks.device)
+    _check("q8_0_split_from_blocks", lib().q8_0_split_from_blocks(_ptr(blocks), _ptr(q), _ptr(d), K, N, _stream(stream)))
+    return q, d
+
+
+def q8_0_blocks_from_split(q, d, blocks=None, stream=None):
+    """(q [N, K] int8, d [N, K/32] fp16 bits) -> ggml Q8_0 blocks (uint8 [N, K/32, 34])."""
+    import torch
+
+    N, K = q.shape
+    if blocks is None:
+        blocks = torch.empty((N, K // 32, 34), dtype=torch.uint8, device=q.device)
+    _check("q8_0_blocks_from_split", lib().q8_0_blocks_from_split(_ptr(q), _ptr(d), _ptr(blocks), K, N, _stream(stream)))
+    return blocks

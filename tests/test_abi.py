@@ -184,6 +184,21 @@ def test_read_probe_checks_its_arguments_on_the_host():
     assert L.w8a8_read_probe(a, 1 << 20, ctypes.c_void_p((1 << 20) + 4), None) == 3
 
 
+def test_quantisation_entry_points_check_arguments_on_the_host():
+    L = lib8.lib()
+    a = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 2)
+    assert L.w8a8_quantize_activations(None, a, a, 16, 4096, None) == 1
+    assert L.w8a8_quantize_activations(a, a, a, 0, 4096, None) == 1
+    assert L.w8a8_quantize_activations(a, a, a, 16, 4100, None) == 2
+    assert L.w8a8_quantize_activations(odd, a, a, 16, 4096, None) == 3
+    assert L.q8_0_quantize(a, a, a, 4010, 320, None) == 2
+    assert L.q8_0_quantize(a, odd, a, 4096, 320, None) == 3
+    assert L.q8_0_split_from_blocks(a, odd, a, 4096, 320, None) == 3
+    assert L.q8_0_split_from_blocks(ctypes.c_void_p((1 << 20) + 1), a, a, 4096, 320, None) == 3
+    assert L.q8_0_blocks_from_split(a, a, a, 4096, 0, None) == 1
+
+
 def test_calls_with_null_pointers_fail_before_any_launch():
     L = lib8.lib()
     null = ctypes.c_void_p(0)
