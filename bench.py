@@ -296,6 +296,81 @@ def time_read_ceiling(dev, nbytes=1 << 30, reps=20):
             "kernel": "w8a8_read_probe (16-byte loads, 2 x SMs x 512 threads)"}
 
 
+def time_graph_calls(make_call, R, calls=256, reps=20):
+    """Median us per call of a CUDA graph of `calls` launches cycling over R buffer sets;
+    make_call(i) issues call i on the current stream."""
+    import torch
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i in range(R):
+            make_call(i)
+    s.synchronize()
+    C = R * max(1, math.ceil(calls / R))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(C):
+            make_call(i % R)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+        s.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e3 / C)
+    del g
+    return statistics.median(times), C
+
+
+def time_quantisation_rows(peak):
+    """The rows after the hot path: activation quantisation (inputs L2-hot, as when produced by the
+    previous kernel), Q8_0 from BF16 and the block re-layout (weights cold: rotating > 3 x L2)."""
+    import torch
+
+    import int8_weight_gemm_gb300 as lib8
+
+    dev = torch.device("cuda")
+    rows = []
+    for (M, K) in ((16, 4096), (32, 12288)):
+        x = torch.randn((M, K), device=dev).to(torch.bfloat16)
+        xq = torch.empty((M, K), dtype=torch.int8, device=dev)
+        xs = torch.empty(M, dtype=torch.float32, device=dev)
+        us, _ = time_graph_calls(lambda i: lib8.w8a8_quantize_activations(x, xq, xs), 1)
+        nbytes = 2 * M * K + M * K + 4 * M
+        rows.append({"op": "w8a8_quantize_activations", "M": M, "K": K, "us_median": round(us, 3),
+                     "bytes": nbytes, "GBps": round(nbytes / us / 1e3, 1), "inputs": "L2-hot"})
+    l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 128 << 20)
+    for (N, K) in ((320, 4096), (4096, 320), (24576, 4096)):
+        wbytes = 2 * N * K
+        R = max(2, math.ceil(3 * l2 / wbytes))
+        ws = [torch.randn((N, K), device=dev).to(torch.bfloat16) for _ in range(R)]
+        q = torch.empty((N, K), dtype=torch.int8, device=dev)
+        d = torch.empty((N, K // 32), dtype=torch.int16, device=dev)
+        us, _ = time_graph_calls(lambda i: lib8.q8_0_quantize(ws[i], q, d), R)
+        nbytes = 2 * N * K + N * K + 2 * N * (K // 32)
+        rows.append({"op": "q8_0_quantize", "N": N, "K": K, "us_median": round(us, 3), "bytes": nbytes,
+                     "GBps": round(nbytes / us / 1e3, 1), "frac_of_measured_hbm": round(nbytes / us / 1e3 / peak, 3),
+                     "rotating_inputs": R})
+        del ws
+        bl = N * (K // 32) * 34
+        R = max(2, math.ceil(3 * l2 / bl))
+        bs = [torch.randint(0, 256, (bl,), dtype=torch.uint8, device=dev) for _ in range(R)]
+        us, _ = time_graph_calls(lambda i: lib8.q8_0_split_from_blocks(bs[i], K, N, q, d), R)
+        rows.append({"op": "q8_0_split_from_blocks", "N": N, "K": K, "us_median": round(us, 3), "bytes": 2 * bl,
+                     "GBps": round(2 * bl / us / 1e3, 1), "frac_of_measured_hbm": round(2 * bl / us / 1e3 / peak, 3),
+                     "rotating_inputs": R})
+        del bs
+        torch.cuda.empty_cache()
+    return rows
+
+
 def time_q8(T, K, N, iters=200, seed=7, flags=0):
     """Median us per Q8_0 read in a graph of calls over rotating weight sets (not L2-resident)."""
     import torch
@@ -415,6 +490,8 @@ def run_ours(args):
             out["q8_0"] = [time_q8(T, K8, N8, flags=f) for (K8, N8) in ((4096, 320), (320, 4096)) for T in (1, 4, 6)
                            for f in (0, lib8.W8A8_FLAG_PDL)]
         out["read_ceiling"] = time_read_ceiling(dev)
+        if not args.no_q8:
+            out["quantisation"] = time_quantisation_rows(peak)
         out["roofline"]["frac_of_read_ceiling"] = round(achieved / out["read_ceiling"]["value"], 4)
         if not args.no_cpu:
             out["cpu_baseline"] = cpu_baseline(M, K, N, x, xs, W, ws)
