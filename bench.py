@@ -35,6 +35,34 @@ KERNEL_SOURCES = ["int8_weight_gemm_gb300/csrc/w8a8_gemm.cu", "int8_weight_gemm_
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "w8a8_gemm_m16_k4096_n1536_traffic.txt")
 
 
+def rank_barrier():
+    """Barrier across the ranks of a torchrun launch (no-op for a single process)."""
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float) -> float:
+    """The largest of the ranks' values (each rank's timed region; the job is as slow as its
+    slowest rank).  NCCL reduces a device tensor, gloo a host one."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world: int, bytes_per_call: int, calls_per_rank: int, total_ms_max: float) -> float:
+    """Whole-job weight-stream GB/s: every rank streams its own replica's weights (weak scaling),
+    timed by the slowest rank."""
+    return world * bytes_per_call * calls_per_rank / (total_ms_max / 1e3) / 1e9
+
+
 def _env_int(name, default):
     try:
         return int(os.environ.get(name, default))
@@ -200,8 +228,7 @@ def time_gemm(M, K, N, dist, seed, steps, warmup, blocks=0, device=None, sample_
     for _ in range(warmup):
         g.replay()
     torch.cuda.synchronize(dev)
-    if torch.distributed.is_available() and torch.distributed.is_initialized():
-        torch.distributed.barrier()
+    rank_barrier()
     torch.cuda.synchronize(dev)
     sampler = ClockSampler(dev.index or 0) if sample_clocks else None
     if sampler:
@@ -216,11 +243,7 @@ def time_gemm(M, K, N, dist, seed, steps, warmup, blocks=0, device=None, sample_
     torch.cuda.synchronize(dev)
     clocks = sampler.stop() if sampler else None
     step_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
-    total_ms = evs[0].elapsed_time(evs[-1])
-    if torch.distributed.is_available() and torch.distributed.is_initialized():
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(evs[0].elapsed_time(evs[-1]))
     per_call_us = sorted(s * 1e3 / C for s in step_ms)
     plan = lib8.w8a8_plan(M, K, N, blocks)
     res = {
@@ -434,8 +457,7 @@ def run_ours(args):
     M, K, N = cfg["M"], cfg["K"], cfg["N"]
     x, xs, W, ws = res.pop("inputs")
     wbytes = res["wbytes"]
-    total_s = res["total_ms"] / 1e3
-    value = world * wbytes * res["launches"] / total_s / 1e9
+    value = whole_job_gbs(world, wbytes, res["launches"], res["total_ms"])
     peak, peak_kind = _peaks()
     alg_bytes = K * N + M * K + 4 * M + 4 * N + 2 * M * N
     achieved = alg_bytes / (res["avg_launch_us"] * 1e-6) / 1e9
@@ -474,7 +496,7 @@ def run_ours(args):
     rp = time_gemm(M, K, N, cfg["dist"], cfg["seed"], min(args.steps, 300), args.warmup, device=dev,
                    want_e2e=False, flags=lib8.W8A8_FLAG_PDL)
     rp.pop("inputs")
-    out["pdl"] = {"value": round(world * wbytes * rp["launches"] / (rp["total_ms"] / 1e3) / 1e9, 2), "unit": "GB/s",
+    out["pdl"] = {"value": round(whole_job_gbs(world, wbytes, rp["launches"], rp["total_ms"]), 2), "unit": "GB/s",
                   "us_per_call": {"median": round(rp["us_median"], 4), "p90": round(rp["us_p90"], 4)},
                   "roofline_frac": round(alg_bytes / (rp["avg_launch_us"] * 1e-6) / 1e9 / peak, 4),
                   "launch": "W8A8_FLAG_PDL, same graph of rotating-weight calls"}
