@@ -248,7 +248,7 @@ def time_gemm(M, K, N, dist, seed, steps, warmup, blocks=0, device=None, sample_
     plan = lib8.w8a8_plan(M, K, N, blocks)
     res = {
         "R": R, "C": C, "wbytes": wbytes, "total_ms": total_ms, "steps": steps,
-        "kernel": f"w8a8_gemm_kernel<{plan['n8_tiles']}, {plan['stages']}>",
+        "kernel": f"w8a8_gemm_kernel<{plan['n8_tiles']}, {plan['stages']}, {str(plan['threads'] == 320).lower()}>",
         "blocks": plan["blocks"],
         "us_median": statistics.median(per_call_us),
         "us_p90": per_call_us[min(len(per_call_us) - 1, int(0.9 * len(per_call_us)))],

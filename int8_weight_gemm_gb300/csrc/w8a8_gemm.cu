@@ -38,7 +38,10 @@ constexpr int kSlabBytes = kTileRows * kKBlock;    // 2048
 constexpr int kConsumerWarps = 8;                  // two per stage slot: even / odd stages
 constexpr int kWarpsPerStage = 4;                  // one slab of a stage each
 constexpr int kSubTiles = 4;                       // 16-row sub-tiles of a 64-row tile
-constexpr int kThreads = 32 * (kConsumerWarps + 1);   // + one producer warp
+constexpr int kThreads = 32 * (kConsumerWarps + 2);   // + one producer warp + one combine warp
+// A launch whose CTAs each finish a single tile segment (the tile-aligned split) has nothing for
+// the combine warp to do and leaves it out.
+constexpr int kThreadsNoCombine = 32 * (kConsumerWarps + 1);
 constexpr int kFlushSlabs = 8;                     // 8 slabs of 32 k = 256 k per warp between int32 flushes
 
 constexpr int kStageSlabs = 4;                     // one slab per consumer warp per stage
@@ -152,6 +155,30 @@ __device__ __forceinline__ int exact_float_to_int(float v) {
   return __float_as_int(__fadd_rn(v, 12582912.0f)) - 0x4B400000;
 }
 
+// Split-tile combine words (see GemmParams::tile_acc).  Two-element word of f-bit fields: the
+// increment of one CTA's partials (a, b), and the decode of a word into the sums a, b of the
+// partials it holds and their count (a = the low f bits sign-extended, b = the next f bits
+// sign-extended after removing a, the count = the rest after removing b).
+__device__ __forceinline__ unsigned long long pair_increment(int va, int vb, int f) {
+  return (1ull << (2 * f)) + ((unsigned long long)(long long)vb << f) + (unsigned long long)(long long)va;
+}
+__device__ __forceinline__ uint32_t pair_decode(unsigned long long w, int f, long long* a, long long* b) {
+  const unsigned long long mask = (1ull << f) - 1ull;
+  const int sh = 64 - f;
+  *a = (long long)((w & mask) << sh) >> sh;
+  const unsigned long long w1 = (w - (unsigned long long)*a) >> f;
+  *b = (long long)((w1 & mask) << sh) >> sh;
+  return (uint32_t)((w1 - (unsigned long long)*b) >> f);
+}
+// One-element word: (arrivals << 52) + the sum of (partial + 2^31); the total of n partials is the
+// low 32 bits minus n * 2^31 (mod 2^32).
+__device__ __forceinline__ unsigned long long single_increment(int v) {
+  return (1ull << 52) + ((uint32_t)v ^ 0x80000000u);
+}
+__device__ __forceinline__ int single_total(unsigned long long old, int v, uint32_t n) {
+  return (int)((uint32_t)old + ((uint32_t)v ^ 0x80000000u) - ((n & 1u) << 31));
+}
+
 // Epilogue of one output element: out[m][n] = bf16_rne((float(acc) * x_scale[m]) * w_scale[n]).
 __device__ __forceinline__ void store_out(const GemmParams& p, int m, int n, int acc, float xsv, float wsv) {
   if (m < p.M && n < p.N) {
@@ -164,10 +191,14 @@ __device__ __forceinline__ void store_out(const GemmParams& p, int m, int n, int
 
 constexpr int kProducerWarp = kConsumerWarps;        // warp 8: lane 0 issues every copy
 constexpr int kProducerThread = 32 * kProducerWarp;
+constexpr int kCombineWarp = kConsumerWarps + 1;     // warp 9: finishes every segment but a CTA's last
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
 
-template <int NT8, int NS>
-__global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_constant__ GemmParams p) {
+template <int NT8, int NS, bool kMulti>
+// kMulti: some CTA finishes more than one tile segment (the run split), so a combine warp finishes
+// every segment but a CTA's last; without it every CTA has exactly one segment.
+__global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
+    w8a8_gemm_kernel(const __grid_constant__ GemmParams p) {
   using L = GemmLayout<NT8, NS>;
   constexpr int kSegInts = L::kSegSumInts / 2;      // one segment-sum buffer
   constexpr int kPer = kSegInts / kConsumerThreads; // output elements per consumer thread at a segment end
@@ -183,7 +214,9 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
   __shared__ __align__(8) uint64_t empty_bar[NS];  // the stage's consumer warps took their slabs
   __shared__ float xs_sm[32];                      // x_scale (0 past M)
   __shared__ float ws_sm[2][kTileRows];            // w_scale of a segment's tile, by segment parity
-  __shared__ __align__(8) uint64_t seg_bar;        // every consumer warp finished the segment
+  __shared__ __align__(8) uint64_t seg_bar;        // every consumer warp finished the CTA's last segment
+  __shared__ __align__(8) uint64_t seg_full[2];    // every consumer warp flushed an earlier segment (by parity)
+  __shared__ __align__(8) uint64_t seg_free[2];    // the combine warp is done with that segment's buffer
   __shared__ int abort_flag;
 
   // 128B-swizzled TMA boxes need a 1 KiB aligned destination.
@@ -214,6 +247,10 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
       mbar_init(&empty_bar[s], kStageWarps);
     }
     mbar_init(&seg_bar, kConsumerWarps);
+    mbar_init(&seg_full[0], kConsumerWarps);
+    mbar_init(&seg_full[1], kConsumerWarps);
+    mbar_init(&seg_free[0], 1);
+    mbar_init(&seg_free[1], 1);
     abort_flag = 0;
     mbar_fence_init();
     // The packed weight is never written by the work this call depends on, so its first stages
@@ -225,9 +262,18 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
       if (!p.pdl) tma_load_2d(xraw + pq * L::kXRawStage, &p.xmap, it.kb0() * kKBlock, 0, &full_bar[pq]);
     }
   }
-  for (int i = threadIdx.x; i < L::kSegSumInts; i += kThreads) segsum[i] = 0;
+  for (int i = threadIdx.x; i < L::kSegSumInts; i += (kMulti ? kThreads : kThreadsNoCombine)) segsum[i] = 0;
   __syncthreads();
   pdl_trigger();   // the next call on the stream may start its own weight prefetch
+
+  // Element e of a segment's sums (layout [sub][j][r][lane]) of tile t, its scales parked in
+  // buffer b: its row m and column n are the inverse of frag_index and of the accumulator fragment
+  // (lane = 4g + c holds rows 2c + (r & 1) of n8 tile j and columns g + 8 (r >> 1) of sub-tile u).
+  auto store_elem = [&](int e, int t, int b, int total) {
+    const int m = 8 * ((e >> 7) % NT8) + 2 * (e & 3) + ((e >> 5) & 1);
+    const int nl = 16 * ((e >> 7) / NT8) + ((e & 31) >> 2) + 8 * ((e >> 6) & 1);
+    store_out(p, m, t * kTileRows + nl, total, xs_sm[m], ws_sm[b][nl]);
+  };
 
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- producer (one thread)
@@ -250,6 +296,85 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
     for (int s = 0; s < NS && s < pq; ++s) {
       const int last = s + NS * ((pq - 1 - s) / NS);
       mbar_wait_drain(&full_bar[s], (uint32_t)((last / NS) & 1), p.status);
+    }
+    return;
+  }
+
+  if (kMulti && warp == kCombineWarp) {
+    // ---------------------------------------------------------------- combine warp
+    // Finishes every segment of this CTA except its last: waits until the consumer warps have
+    // flushed the segment's sums, stores a whole tile directly or adds a split tile's partials
+    // into its workspace words (storing the elements this CTA completes), clears the sums and
+    // hands the buffer back.  The consumer warps stream on meanwhile; the last segment, after
+    // which there is nothing left to stream, they finish themselves.
+    pdl_wait();   // out and the workspace words may belong to the previous call
+    int s = 0;
+    for (int seg_begin = b0, seg_end = 0; seg_begin < b1; seg_begin = seg_end, ++s) {
+      const int t = seg_begin / p.KB;
+      seg_end = min(b1, (t + 1) * p.KB);
+      if (seg_end == b1) break;
+      const int buf = s & 1;
+      if (!mbar_wait(&seg_full[buf], (uint32_t)((s >> 1) & 1), &abort_flag, p.status)) return;
+      int* const sums = segsum + buf * kSegInts;
+      unsigned long long* const tacc = p.tile_acc + (size_t)t * kSegInts;
+      const uint32_t n = (uint32_t)gemm_split_contributors(p.split, t);
+      if (seg_begin == t * p.KB) {   // the whole tile is ours (it ends before b1, so it is complete)
+        for (int e = lane; e < kSegInts; e += 32) {
+          store_elem(e, t, buf, sums[e]);
+          sums[e] = 0;
+        }
+      } else if (p.pack_f) {
+        constexpr int kHalf = kSegInts / 2, kWords = kHalf / 32;   // words of this lane: lane + 32 w
+        for (int w0 = 0; w0 < kWords; w0 += 8) {
+          unsigned long long old[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int i = lane + 32 * (w0 + k);
+            if (w0 + k < kWords) old[k] = atom_add_relaxed_u64(tacc + i, pair_increment(sums[i], sums[i + kHalf], p.pack_f));
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int i = lane + 32 * (w0 + k);
+            if (w0 + k >= kWords) break;
+            long long a, bb;
+            const uint32_t arrived = pair_decode(old[k], p.pack_f, &a, &bb);
+            if (arrived == n - 1) {
+              tacc[i] = 0ull;
+              store_elem(i, t, buf, (int)(a + sums[i]));
+              store_elem(i + kHalf, t, buf, (int)(bb + sums[i + kHalf]));
+            } else if (arrived >= n) {
+              atomicOr(p.status, W8A8_DEV_COUNTER_CORRUPT);
+            }
+            sums[i] = 0;
+            sums[i + kHalf] = 0;
+          }
+        }
+      } else {
+        constexpr int kElems = kSegInts / 32;
+        for (int w0 = 0; w0 < kElems; w0 += 8) {
+          unsigned long long old[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int e = lane + 32 * (w0 + k);
+            if (w0 + k < kElems) old[k] = atom_add_relaxed_u64(tacc + e, single_increment(sums[e]));
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int e = lane + 32 * (w0 + k);
+            if (w0 + k >= kElems) break;
+            const uint32_t arrived = (uint32_t)(old[k] >> 52);
+            if (arrived == n - 1) {
+              tacc[e] = 0ull;
+              store_elem(e, t, buf, single_total(old[k], sums[e], n));
+            } else if (arrived >= n) {
+              atomicOr(p.status, W8A8_DEV_COUNTER_CORRUPT);
+            }
+            sums[e] = 0;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&seg_free[buf]);
     }
     return;
   }
@@ -297,67 +422,8 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
         }
   };
 
-  // Output element i of this thread at a segment end: element e = threadIdx.x + kConsumerThreads * i
-  // of the segment sums (layout [sub][j][r][lane]).  Its row m and column n are the inverse of
-  // frag_index and of the accumulator fragment (lane = 4g + c holds rows 2c + (r & 1) of n8 tile j
-  // and columns g + 8 (r >> 1) of sub-tile u).
-  auto finish = [&](int i, int t, int b, int total) {
-    const int e = threadIdx.x + kConsumerThreads * i;
-    const int m = 8 * ((e >> 7) % NT8) + 2 * (e & 3) + ((e >> 5) & 1);
-    const int nl = 16 * ((e >> 7) / NT8) + ((e & 31) >> 2) + 8 * ((e >> 6) & 1);
-    store_out(p, m, t * kTileRows + nl, total, xs_sm[m], ws_sm[b][nl]);
-  };
-  // A split segment whose atomics are in flight: tile, sum buffer, contributor count, results.
-  bool pending = false;
-  int pend_t = 0, pend_buf = 0;
-  uint32_t pend_n = 0;
-  unsigned long long pend_old[kPer];
-  auto resolve = [&]() {
-    int* const pm = segsum + pend_buf * kSegInts + threadIdx.x;
-    unsigned long long* const tacc = p.tile_acc + (size_t)pend_t * kSegInts + threadIdx.x;
-    if (p.pack_f) {
-      const int pf = p.pack_f;
-      // Element pair (i, i + kPer / 2) shares word i.  The old word holds the sums a, b of the
-      // partials added before this CTA's and their count c: a = the low f bits sign-extended,
-      // b = the next f bits sign-extended after removing a, c = the rest after removing b.
-      const unsigned long long mask = (1ull << pf) - 1ull;
-      const int sh = 64 - pf;
-#pragma unroll
-      for (int i = 0; i < kPer / 2; ++i) {
-        const unsigned long long w = pend_old[i];
-        const long long a = (long long)((w & mask) << sh) >> sh;
-        const unsigned long long w1 = (w - (unsigned long long)a) >> pf;
-        const long long bb = (long long)((w1 & mask) << sh) >> sh;
-        const uint32_t arrived = (uint32_t)((w1 - (unsigned long long)bb) >> pf);
-        const int va = pm[kConsumerThreads * i];
-        const int vb = pm[kConsumerThreads * (i + kPer / 2)];
-        pm[kConsumerThreads * i] = 0;
-        pm[kConsumerThreads * (i + kPer / 2)] = 0;
-        if (arrived == pend_n - 1) {
-          tacc[kConsumerThreads * i] = 0ull;
-          finish(i, pend_t, pend_buf, (int)(a + va));
-          finish(i + kPer / 2, pend_t, pend_buf, (int)(bb + vb));
-        } else if (arrived >= pend_n) {
-          atomicOr(p.status, W8A8_DEV_COUNTER_CORRUPT);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const uint32_t arrived = (uint32_t)(pend_old[i] >> 52);
-        const uint32_t biased = (uint32_t)pm[kConsumerThreads * i] ^ 0x80000000u;
-        pm[kConsumerThreads * i] = 0;
-        if (arrived == pend_n - 1) {
-          tacc[kConsumerThreads * i] = 0ull;
-          // the biased sum minus n * 2^31, mod 2^32
-          finish(i, pend_t, pend_buf, (int)((uint32_t)pend_old[i] + biased - ((pend_n & 1u) << 31)));
-        } else if (arrived >= pend_n) {
-          atomicOr(p.status, W8A8_DEV_COUNTER_CORRUPT);
-        }
-      }
-    }
-    pending = false;
-  };
+  // Output element i of this thread at the last segment's end: e = threadIdx.x + kConsumerThreads * i.
+  auto finish = [&](int i, int t, int b, int total) { store_elem(threadIdx.x + kConsumerThreads * i, t, b, total); };
 
   // Offsets of this warp's fragments inside a stage (the same for every stage): W fragments of
   // its sub-tiles in its slab; row g of the activation box sits at g * 128 with its 16-byte chunks
@@ -375,8 +441,11 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
     const int seg_slabs = seg_end - seg_begin;
     const int seg_stages = (seg_slabs + kStageSlabs - 1) / kStageSlabs;
     // Start of a segment: count the tile's contributors and fetch its w_scale now, off the
-    // segment's tail.
+    // segment's tail.  The sum buffer of this segment's parity is free once the combine warp has
+    // finished the segment two before (the last segment never shares its buffer with a later one).
     arrivals = (uint32_t)gemm_split_contributors(p.split, t);
+    if (kMulti && segs >= 2 && !mbar_wait(&seg_free[segs & 1], (uint32_t)(((segs - 2) >> 1) & 1), &abort_flag, p.status))
+      return;
     if (threadIdx.x < kTileRows) {
       const int n = t * kTileRows + (int)threadIdx.x;
       ws_reg = n < p.N ? __ldg(p.w_scale + n) : 0.f;
@@ -439,59 +508,66 @@ __global__ void __launch_bounds__(kThreads, 2) w8a8_gemm_kernel(const __grid_con
     if (since) flush(sums);
     since = 0;
     ++segs;
-    // The previous split segment's atomics were issued one segment ago: their results are back.
-    // Its sum buffer and scales stay untouched until after the barrier below.
-    if (pending) resolve();
-    // Every consumer's part is in the sums, and the scales are in shared memory.  Both buffers are
-    // next written two segments later, after the next segment's barrier, which each thread reaches
-    // only after its reads and clears here (a split segment's reads and clears happen at the next
-    // segment end, before that barrier, or after the loop).
-    // The barrier is an mbarrier wait, bounded like every other wait (a warp that gave up on a
-    // timeout never arrives, and the others then give up too).
+    if (kMulti && seg_end != b1) {
+      // An earlier segment: hand it to the combine warp and stream on.
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&seg_full[buf]);
+      continue;
+    }
+    // The last segment: every consumer's part is in the sums and the scales are in shared memory
+    // once all consumer warps have met (an mbarrier wait, bounded like every other: a warp that
+    // gave up on a timeout never arrives, and the others then give up too).  The consumers finish
+    // it together, every thread kPer elements.
     __syncwarp();
     if (lane == 0) mbar_arrive(&seg_bar);
-    if (!mbar_wait(&seg_bar, (uint32_t)((segs - 1) & 1), &abort_flag, p.status)) return;
+    if (!mbar_wait(&seg_bar, 0u, &abort_flag, p.status)) return;
     int* const mine = sums + threadIdx.x;   // element i at mine[kConsumerThreads * i]
     if (seg_begin == t * p.KB && seg_end == (t + 1) * p.KB) {   // the whole tile is ours
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        finish(i, t, buf, mine[kConsumerThreads * i]);
-        mine[kConsumerThreads * i] = 0;
-      }
-      continue;
+      for (int i = 0; i < kPer; ++i) finish(i, t, buf, mine[kConsumerThreads * i]);
+      break;
     }
-    // Split tile.  Each element's word counts its arrivals in bits 52..63 and sums the partials,
-    // each offset by 2^31 so that it is a non-negative 32-bit number, in bits 0..51 (at most 2048
-    // CTAs share a tile, so neither field overflows).  int32 addition is associative, so the CTA
-    // that brings the count to n holds the same total, in the same bits, as an ascending-order
-    // sum of the n partials; it stores the bf16 result and returns the word to zero for the next
-    // call.  One returning atomic per element: no separate counter, fence or read-back.  The
-    // results are examined one segment later (or after the last one), so the consumers go on
-    // streaming while the atomics travel.
+    // Split tile.  Each contributor adds its partials into the elements' workspace words with one
+    // returning atomic per word; the contributor that brings a word's count to n holds the same
+    // total, in the same bits, as an ascending-order sum of the n partials (int32 addition is
+    // associative), stores the bf16 result and returns the word to zero for the next call.  No
+    // separate counter, fence or read-back.  Two elements share a word when the fields fit
+    // (pack_f), halving the atomics.
     unsigned long long* const tacc = p.tile_acc + (size_t)t * kSegInts + threadIdx.x;
     if (p.pack_f) {
-      const int pf = p.pack_f;
-      // Two elements per word: half as many atomics (their number, not contention, bounds the
-      // combine's time).
+      unsigned long long old[kPer / 2];
+#pragma unroll
+      for (int i = 0; i < kPer / 2; ++i)
+        old[i] = atom_add_relaxed_u64(tacc + kConsumerThreads * i,
+                                      pair_increment(mine[kConsumerThreads * i], mine[kConsumerThreads * (i + kPer / 2)], p.pack_f));
 #pragma unroll
       for (int i = 0; i < kPer / 2; ++i) {
-        const long long va = mine[kConsumerThreads * i];
-        const long long vb = mine[kConsumerThreads * (i + kPer / 2)];
-        const unsigned long long inc = (1ull << (2 * pf)) + ((unsigned long long)vb << pf) + (unsigned long long)va;
-        pend_old[i] = atom_add_relaxed_u64(tacc + kConsumerThreads * i, inc);
+        long long a, bb;
+        const uint32_t arrived = pair_decode(old[i], p.pack_f, &a, &bb);
+        if (arrived == arrivals - 1) {
+          tacc[kConsumerThreads * i] = 0ull;
+          finish(i, t, buf, (int)(a + mine[kConsumerThreads * i]));
+          finish(i + kPer / 2, t, buf, (int)(bb + mine[kConsumerThreads * (i + kPer / 2)]));
+        } else if (arrived >= arrivals) {
+          atomicOr(p.status, W8A8_DEV_COUNTER_CORRUPT);
+        }
       }
     } else {
+      unsigned long long old[kPer];
 #pragma unroll
-      for (int i = 0; i < kPer; ++i)
-        pend_old[i] = atom_add_relaxed_u64(tacc + kConsumerThreads * i,
-                                           (1ull << 52) + ((uint32_t)mine[kConsumerThreads * i] ^ 0x80000000u));
+      for (int i = 0; i < kPer; ++i) old[i] = atom_add_relaxed_u64(tacc + kConsumerThreads * i, single_increment(mine[kConsumerThreads * i]));
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const uint32_t arrived = (uint32_t)(old[i] >> 52);
+        if (arrived == arrivals - 1) {
+          tacc[kConsumerThreads * i] = 0ull;
+          finish(i, t, buf, single_total(old[i], mine[kConsumerThreads * i], arrivals));
+        } else if (arrived >= arrivals) {
+          atomicOr(p.status, W8A8_DEV_COUNTER_CORRUPT);
+        }
+      }
     }
-    pending = true;
-    pend_t = t;
-    pend_buf = buf;
-    pend_n = arrivals;
   }
-  if (pending) resolve();
 }
 
 // --------------------------------------------------------------------------------------------
@@ -553,7 +629,7 @@ int gemm_plan(int M, int K, int N, int blocks, int sm_count, GemmPlan* plan) {
     }
     pl.pack_f = (count_bits >= 1 && count_bits < 63 && (long long)most < (1ll << count_bits)) ? f : 0;
   }
-  pl.threads = kThreads;
+  pl.threads = pl.blocks >= pl.n_tiles ? kThreadsNoCombine : kThreads;
   pl.stage_slabs = kStageSlabs;
   pl.stages = gemm_stages(pl.nt8);
   pl.smem_bytes = gemm_smem_bytes(pl.nt8);
@@ -565,15 +641,15 @@ int gemm_plan(int M, int K, int N, int blocks, int sm_count, GemmPlan* plan) {
   return W8A8_OK;
 }
 
-template <int NT8, int NS>
-static cudaError_t launch_gemm(const GemmParams& p, int blocks, bool pdl, cudaStream_t stream) {
-  auto kern = w8a8_gemm_kernel<NT8, NS>;
+template <int NT8, int NS, bool kMulti>
+static cudaError_t launch_gemm(const GemmParams& p, int blocks, int threads, bool pdl, cudaStream_t stream) {
+  auto kern = w8a8_gemm_kernel<NT8, NS, kMulti>;
   const int smem = GemmLayout<NT8, NS>::kBytes;
   cudaError_t e = ensure_smem_attribute((const void*)kern, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3((unsigned)threads);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -610,11 +686,16 @@ cudaError_t gemm_launch(const GemmPlan& pl, const int8_t* x, const float* xs, co
   p.split = make_gemm_split(pl.n_tiles, pl.kb, pl.blocks);
   p.pack_f = pl.pack_f;
   p.pdl = pdl ? 1 : 0;
+  const bool multi = pl.threads == kThreads;
   switch (pl.nt8) {
-    case 1: return launch_gemm<1, kStages1>(p, pl.blocks, pdl, stream);
-    case 2: return launch_gemm<2, kStages2>(p, pl.blocks, pdl, stream);
-    case 3: return launch_gemm<3, kStages3>(p, pl.blocks, pdl, stream);
-    default: return launch_gemm<4, kStages4>(p, pl.blocks, pdl, stream);
+    case 1: return multi ? launch_gemm<1, kStages1, true>(p, pl.blocks, pl.threads, pdl, stream)
+                         : launch_gemm<1, kStages1, false>(p, pl.blocks, pl.threads, pdl, stream);
+    case 2: return multi ? launch_gemm<2, kStages2, true>(p, pl.blocks, pl.threads, pdl, stream)
+                         : launch_gemm<2, kStages2, false>(p, pl.blocks, pl.threads, pdl, stream);
+    case 3: return multi ? launch_gemm<3, kStages3, true>(p, pl.blocks, pl.threads, pdl, stream)
+                         : launch_gemm<3, kStages3, false>(p, pl.blocks, pl.threads, pdl, stream);
+    default: return multi ? launch_gemm<4, kStages4, true>(p, pl.blocks, pl.threads, pdl, stream)
+                          : launch_gemm<4, kStages4, false>(p, pl.blocks, pl.threads, pdl, stream);
   }
 }
 

@@ -113,6 +113,8 @@ def test_plan_shape_and_limits():
     assert p["n8_tiles"] == 2 and p["n_tiles"] == 24 and p["k_blocks"] == 128
     assert p["blocks"] == 304                                   # two CTAs per SM (152 SMs without a GPU)
     assert lib8.w8a8_plan(1, 512, 256)["blocks"] == 64           # never more CTAs than slabs
+    # a combine warp only when some CTA finishes more than one tile segment (fewer CTAs than tiles)
+    assert p["threads"] == 288 and lib8.w8a8_plan(16, 4096, 24576)["threads"] == 320
     assert p["smem_bytes"] * 2 <= 228 * 1024          # two CTAs per SM fit
     for M in (1, 8, 9, 16, 17, 24, 25, 32):
         q = lib8.w8a8_plan(M, 4096, 1536)
