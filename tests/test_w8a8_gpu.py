@@ -260,3 +260,19 @@ def test_read_probe_runs_and_leaves_its_input_alone():
     lib8.w8a8_read_probe(buf, sink)
     torch.cuda.synchronize()
     assert torch.equal(buf, ref)
+
+
+@pytest.mark.parametrize("K,N,blocks", [(65536, 256, 3), (65536, 256, 1), (4096, 256, 3)])
+def test_multi_segment_ctas_with_both_word_formats(K, N, blocks):
+    # Fewer CTAs than tiles: each CTA streams a run across several tiles, and the combine warp
+    # finishes every segment but a CTA's last.  K = 65536 leaves no room for two elements per word
+    # (one-element words); K = 4096 uses two-element words.
+    M = 5
+    x, xs, W, ws = synth.w8a8_inputs(M, K, N, seed=K + blocks)
+    plan = lib8.w8a8_plan(M, K, N, blocks)
+    assert plan["threads"] == 320
+    assert plan["combine_pack_bits"] == (0 if K == 65536 else 28)
+    case = W8A8Case(x, xs, W, ws, blocks=blocks)
+    _check(case, x, xs, W, ws)
+    torch.cuda.synchronize()
+    assert (case.ws[4:] == 0).all()
