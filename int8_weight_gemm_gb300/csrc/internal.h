@@ -29,7 +29,9 @@ struct Q8Plan {
   int kb;            // K / 32
   int warps;         // warps per CTA (each a contiguous run of k blocks)
   int splits;        // CTAs per tile along K (combined by the last arrival)
-  int blocks;        // n_tiles * splits
+  int cluster;       // > 1: the tile's warps spread over a cluster of this many CTAs (splits == 1)
+  int tile_warps;    // warps per tile (the k-block runs; equals warps unless cluster > 1)
+  int blocks;        // n_tiles * splits * cluster
   size_t workspace_bytes, counters_offset, partials_offset;
 };
 

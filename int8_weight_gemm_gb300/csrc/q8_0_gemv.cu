@@ -35,6 +35,8 @@ struct Q8Params {
   uint32_t* counters;
   float4* partials;
   int T, K, N, KB, warps, splits;
+  int cluster;      // > 1: CTA r of a tile's cluster runs the tile's warps r * warps .. r * warps + warps - 1
+  int tile_warps;   // warps of a tile in all (the k-block runs)
 };
 
 // Two signed int8 (bytes i0, i1 of v) -> bf16x2 (i0 in the low half), exact.  In offset binary
@@ -61,12 +63,16 @@ __global__ void __launch_bounds__(32 * kQ8MaxWarps) q8_0_gemv_kernel(const __gri
   __shared__ float4 red[kQ8MaxWarps][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int tile = blockIdx.x / p.splits;
-  const int split = blockIdx.x % p.splits;
+  const int rank = p.cluster > 1 ? (int)cluster_ctarank() : 0;
+  const int tile = blockIdx.x / (p.splits * p.cluster);
+  const int split = (blockIdx.x / p.cluster) % p.splits;
   const int cb0 = even_lo(split, p.KB, p.splits);
   const int cb1 = even_lo(split + 1, p.KB, p.splits);
-  const int wb0 = cb0 + even_lo(warp, cb1 - cb0, p.warps);
-  const int wb1 = cb0 + even_lo(warp + 1, cb1 - cb0, p.warps);
+  // This warp's run of k blocks: the tile's warps split the split's blocks into equal runs, and a
+  // cluster spreads them over its CTAs (a warp past the tile's count has none).
+  const int tw = rank * p.warps + warp;
+  const int wb0 = cb0 + even_lo(min(tw, p.tile_warps), cb1 - cb0, p.tile_warps);
+  const int wb1 = cb0 + even_lo(min(tw + 1, p.tile_warps), cb1 - cb0, p.tile_warps);
   const int nb = wb1 - wb0;
   const int n_a = tile * 16 + g, n_b = n_a + 8;
 
@@ -143,11 +149,20 @@ __global__ void __launch_bounds__(32 * kQ8MaxWarps) q8_0_gemv_kernel(const __gri
     }
   }
 
-  red[warp][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  __syncthreads();
-  if (warp != 0) return;
+  if (p.cluster > 1) {
+    // The tile's warp partials gather in CTA 0 of the cluster (distributed shared memory), which
+    // sums them in warp order, exactly as one CTA holding all the tile's warps would.
+    if (tw < p.tile_warps)
+      st_cluster_v4f(cluster_map(smem_addr(&red[tw][lane]), 0u), make_float4(acc[0], acc[1], acc[2], acc[3]));
+    cluster_sync_all();
+    if (rank != 0 || warp != 0) return;
+  } else {
+    red[warp][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    __syncthreads();
+    if (warp != 0) return;
+  }
   float tot[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int w = 0; w < p.warps; ++w) {
+  for (int w = 0; w < p.tile_warps; ++w) {
     const float4 v = red[w][lane];
     tot[0] += v.x;
     tot[1] += v.y;
@@ -206,7 +221,16 @@ int q8_plan(int T, int K, int N, Q8Plan* plan) {
   const int per_split = (pl.kb + pl.splits - 1) / pl.splits;
   const int warps = (per_split + kQ8TargetBlocksPerWarp - 1) / kQ8TargetBlocksPerWarp;
   pl.warps = warps < kQ8MaxWarps ? warps : kQ8MaxWarps;   // then at most 8 blocks per warp
-  pl.blocks = pl.n_tiles * pl.splits;
+  // A tile read by one CTA with four or more warps spreads its warps over a cluster, two per CTA:
+  // more SMs pull the weight, the partials meet in distributed shared memory in the same order,
+  // and the sums are bit-identical to the one-CTA read.
+  pl.tile_warps = pl.warps;
+  pl.cluster = 1;
+  if (pl.splits == 1 && pl.warps >= 4) {
+    pl.cluster = (pl.warps + 1) / 2;
+    pl.warps = 2;
+  }
+  pl.blocks = pl.n_tiles * pl.splits * pl.cluster;
   const size_t counters = ((size_t)pl.n_tiles * 4 + 255) / 256 * 256;
   const size_t partials = pl.splits > 1 ? (size_t)pl.n_tiles * pl.splits * 32 * 16 : 0;
   pl.counters_offset = kWsHeaderBytes;
@@ -232,16 +256,29 @@ cudaError_t q8_launch(const Q8Plan& pl, const void* x, const int8_t* q, const vo
   p.KB = pl.kb;
   p.warps = pl.warps;
   p.splits = pl.splits;
+  p.cluster = pl.cluster;
+  p.tile_warps = pl.tile_warps;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)pl.blocks);
   cfg.blockDim = dim3((unsigned)(32 * pl.warps));
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (pl.cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)pl.cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = n;
   cudaError_t e = cudaLaunchKernelEx(&cfg, q8_0_gemv_kernel, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
