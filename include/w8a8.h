@@ -4,9 +4,12 @@
  * Two operators of an LLM serving engine's decode and speculative-verify windows:
  *
  *  w8a8_gemm   x_q[M,K] int8 @ W[K,N] int8 -> int32, then * x_scale[M] * w_scale[N] -> bf16[M,N],
- *              M <= 32.  Defined by the operator line of "INT8 W8A8 GEMM - Decode (M <= 32) -
+ *              M <= 128.  Defined by the operator line of "INT8 W8A8 GEMM - Decode (M <= 32) -
  *              gfx928 / SGLang TP4" (header paragraph); split-K with a fused last-arrival combine
- *              follows its section 1.1 (qkv recipe) and "Cross-shape rules that held".
+ *              follows its section 1.1 (qkv recipe) and "Cross-shape rules that held".  M <= 32
+ *              runs the decode arm; 32 < M <= 128 runs a second, staged arm on the tcgen05 tensor
+ *              cores over the same packed weight (that page's section 3 keeps such an arm beside
+ *              the decode one for the same (K, N)).
  *  q8_0_gemv   y[T,N] = x[T,K] (bf16) times Q8_0 weights (blocks of 32 int8 quants along K with one
  *              fp16 scale each), T <= 8, bf16 out.  Defined by "sycl: STRATA_HC_Q8=1 reads the Q8_0
  *              hyper-connection projections", section "What changed" (w = d * q, the split layout,
@@ -99,10 +102,12 @@ int w8a8_workspace_status(void* ws, size_t ws_bytes, void* stream, uint32_t* sta
 /* Bytes of the packed weight for a [K,N] int8 W: 64 * ceil(N/64) * K. */
 size_t w8a8_packed_weight_bytes(int K, int N);
 
-/* Workspace bytes that w8a8_gemm needs for every M in [1, M_max] at this (K, N) and `blocks`
- * (0 = the automatic plan, whose CTA count follows the current device's SM count).  Returns 0
- * for arguments w8a8_gemm would reject.  Layout: a 256-byte header (status word first), then
- * one 64-bit accumulator word per output element of every 64-row tile (zero between calls). */
+/* Workspace bytes that w8a8_gemm needs for every M in [1, M_max] (M_max <= 128) at this (K, N)
+ * and `blocks` (0 = the automatic plan, whose CTA count follows the current device's SM count).
+ * Returns 0 for arguments w8a8_gemm would reject.  Layout: a 256-byte header (status word first),
+ * then, for M <= 32, one 64-bit accumulator word per output element of every 64-row tile; for
+ * M > 32, one 32-bit arrival counter per 128-row tile (padded to 256 bytes) and one int32 sum
+ * per (tile, activation row < 64 or 128, tile row).  All of it is zero between calls. */
 size_t w8a8_workspace_bytes(int M_max, int K, int N, int blocks);
 
 /* Pack W once, at load time and outside any timed region or capture (section 1.1 of the W8A8
@@ -130,7 +135,7 @@ int w8a8_pack_weights(const int8_t* W, int K, int N, void* W_packed, void* ws, s
  *  W_packed from w8a8_pack_weights(W, K, N, ...).      w_scale  [N] fp32.
  *  out      [M,N] bf16 row-major (uint16_t storage), 16-byte aligned; rows m >= M and columns
  *           n >= N are never written.
- *  M in [1, 32]; K % 32 == 0; N % 8 == 0 (same limits as the pack).
+ *  M in [1, 128]; K % 32 == 0; N % 8 == 0 (same limits as the pack).
  *  blocks   number of CTAs that share the T = ceil(N/64) tiles x KB = K/32 slabs of 2 KiB
  *           (split-K generalised; every cut lies on a 32-aligned k).  With blocks >= T each tile
  *           is cut into c + 1 (the first blocks % T tiles) or c = blocks / T contiguous parts of
@@ -138,6 +143,8 @@ int w8a8_pack_weights(const int8_t* W, int K, int N, void* W_packed, void* ws, s
  *           blocks < T the tiles are laid end to end and CTA i takes a contiguous run of
  *           ceil or floor(T KB / blocks) slabs (the longer runs first).  0 = automatic (twice
  *           the SM count, at most one CTA per slab).  Must not exceed the number of slabs.
+ *           For M > 32 the same rule applies to T = ceil(N/128) tiles of 128 rows (two packed
+ *           tiles each) x KB units of 32 k, with one CTA per SM by default.
  *  flags    0 or W8A8_FLAG_PDL; any other bit is INVALID_ARG.
  *  ws       workspace of at least w8a8_workspace_bytes(M, K, N, blocks) bytes.
  *  The int32 sums are exact (the result does not depend on `blocks`), and the epilogue order is
@@ -149,10 +156,10 @@ int w8a8_gemm(const int8_t* x_q, const float* x_scale, const void* W_packed, con
 
 /* Launch plan of a w8a8_gemm call (host-only query; launches nothing). */
 typedef struct {
-    int n8_tiles;          /* MMA column tiles of 8 covering M: 1..4 */
-    int n_tiles;           /* 64-row tiles of N */
+    int n8_tiles;          /* column tiles of 8 covering M: 1..4, or 8 / 16 (MMA N = 64 / 128) */
+    int n_tiles;           /* tiles of N (tile_rows rows each) */
     int k_blocks;          /* K / 32 */
-    long long slabs;       /* n_tiles * k_blocks (2 KiB of packed weight each) */
+    long long slabs;       /* n_tiles * k_blocks: the split's units (32 k of one tile each) */
     int blocks;            /* CTAs launched */
     int threads;           /* threads per CTA */
     int stage_slabs;       /* slabs per pipeline stage */
@@ -162,6 +169,8 @@ typedef struct {
     int combine_pack_bits; /* split-tile combine: 0 = one output element per 64-bit workspace word,
                               f > 0 = two elements per word in f-bit fields plus a 64 - 2f bit
                               arrival count (chosen when both fit; halves the atomics) */
+    int tile_rows;         /* weight rows per tile: 64 (M <= 32) or 128 (M > 32) */
+    int tensor_memory;     /* 1: the tcgen05 arm (accumulators in tensor memory), 0: the decode arm */
 } w8a8_plan_t;
 
 int w8a8_plan(int M, int K, int N, int blocks, w8a8_plan_t* plan);
@@ -171,7 +180,10 @@ int w8a8_plan(int M, int K, int N, int blocks, w8a8_plan_t* plan);
  * [32 (u % KB), 32 (u % KB) + 32)).  n_bounds must be blocks + 1.  Host-only. */
 int w8a8_split_bounds(int K, int N, int blocks, long long* bounds, int n_bounds);
 
-/* W8A8 decode GEMM that allocates nothing and takes no workspace.  The pages have no counterpart:
+/* The same for the plan of an M-row call (M > 32: units of 32 k of a 128-row tile). */
+int w8a8_split_bounds_m(int M, int K, int N, int blocks, long long* bounds, int n_bounds);
+
+/* W8A8 GEMM (both arms) that allocates nothing and takes no workspace.  The pages have no counterpart:
  * this entry point exists for callers that cannot provide device memory, such as a plugin that
  * sees only the input and output pointers its host engine hands it, or a request path that must
  * not call cudaMalloc (which can synchronise the device and stall other streams).

@@ -58,6 +58,8 @@ class PlanT(ctypes.Structure):
         ("smem_bytes", ctypes.c_size_t),
         ("workspace_bytes", ctypes.c_size_t),
         ("combine_pack_bits", ctypes.c_int),
+        ("tile_rows", ctypes.c_int),
+        ("tensor_memory", ctypes.c_int),
     ]
 
 
@@ -74,6 +76,7 @@ SIGNATURES = {
     "w8a8_gemm_no_alloc": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_i, _c_i, _c_i, _c_i, ctypes.c_uint, _c_p], _c_i),
     "w8a8_plan": ([_c_i, _c_i, _c_i, _c_i, ctypes.POINTER(PlanT)], _c_i),
     "w8a8_split_bounds": ([_c_i, _c_i, _c_i, ctypes.POINTER(ctypes.c_longlong), _c_i], _c_i),
+    "w8a8_split_bounds_m": ([_c_i, _c_i, _c_i, _c_i, ctypes.POINTER(ctypes.c_longlong), _c_i], _c_i),
     "q8_0_workspace_bytes": ([_c_i, _c_i, _c_i], _c_sz),
     "w8a8_read_probe": ([_c_p, _c_sz, _c_p, _c_p], _c_i),
     "w8a8_quantize_activations": ([_c_p, _c_p, _c_p, _c_i, _c_i, _c_p], _c_i),
@@ -162,10 +165,13 @@ def w8a8_plan(M: int, K: int, N: int, blocks: int = 0) -> dict:
     return {f: getattr(p, f) for f, _ in PlanT._fields_}
 
 
-def w8a8_split_bounds(K: int, N: int, blocks: int) -> list:
+def w8a8_split_bounds(K: int, N: int, blocks: int, M: int = 1) -> list:
     n = blocks + 1
     arr = (ctypes.c_longlong * n)()
-    _check("w8a8_split_bounds", lib().w8a8_split_bounds(K, N, blocks, arr, n))
+    if M == 1:
+        _check("w8a8_split_bounds", lib().w8a8_split_bounds(K, N, blocks, arr, n))
+    else:
+        _check("w8a8_split_bounds_m", lib().w8a8_split_bounds_m(M, K, N, blocks, arr, n))
     return list(arr)
 
 

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libw8a8_gb300.so")
-SOURCES = ["api.cu", "w8a8_gemm.cu", "q8_0_gemv.cu", "no_alloc.cu", "read_probe.cu", "quantize.cu"]
+SOURCES = ["api.cu", "w8a8_gemm.cu", "w8a8_gemm_tc.cu", "q8_0_gemv.cu", "no_alloc.cu", "read_probe.cu", "quantize.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr", "-Xptxas", "-v"]
 

@@ -84,6 +84,17 @@ cudaError_t encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType type, voi
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+int any_plan(int M, int K, int N, int blocks, int sm_count, AnyPlan* plan) {
+  plan->tc = M > kDecodeMaxM;
+  return plan->tc ? tc_plan(M, K, N, blocks, sm_count, &plan->t) : gemm_plan(M, K, N, blocks, sm_count, &plan->g);
+}
+
+cudaError_t any_launch(const AnyPlan& pl, const int8_t* x, const float* xs, const void* wp, const float* wsc, void* out,
+                       int M, int K, int N, void* ws, bool pdl, cudaStream_t stream) {
+  return pl.tc ? tc_launch(pl.t, x, xs, wp, wsc, out, M, K, N, ws, pdl, stream)
+               : gemm_launch(pl.g, x, xs, wp, wsc, out, M, K, N, ws, pdl, stream);
+}
+
 }  // namespace w8a8
 
 using namespace w8a8;
@@ -134,24 +145,46 @@ size_t w8a8_packed_weight_bytes(int K, int N) {
 }
 
 size_t w8a8_workspace_bytes(int M_max, int K, int N, int blocks) {
-  if (M_max < 1 || M_max > 32) return 0;
+  if (M_max < 1 || M_max > kTcMaxM) return 0;
   const int sms = current_sm_count();
   size_t best = 0;
-  for (int m = 1; m <= M_max; m += 8) {   // one plan per n8-tile count
-    GemmPlan pl;
-    if (gemm_plan(m, K, N, blocks, sms, &pl) != W8A8_OK) return 0;
-    if (pl.workspace_bytes > best) best = pl.workspace_bytes;
+  // One plan per kernel variant that some M in [1, M_max] runs: the decode arm's n8-tile counts,
+  // then the tensor-memory arm's two MMA widths.
+  const int probes[] = {1, 9, 17, 25, 32, 33, 64, 65, 128};
+  for (int m : probes) {
+    if (m > M_max) break;
+    AnyPlan pl;
+    if (any_plan(m, K, N, blocks, sms, &pl) != W8A8_OK) return 0;
+    if (pl.workspace_bytes() > best) best = pl.workspace_bytes();
   }
-  GemmPlan pl;
-  if (gemm_plan(M_max, K, N, blocks, sms, &pl) != W8A8_OK) return 0;
-  return pl.workspace_bytes > best ? pl.workspace_bytes : best;
+  AnyPlan pl;
+  if (any_plan(M_max, K, N, blocks, sms, &pl) != W8A8_OK) return 0;
+  return pl.workspace_bytes() > best ? pl.workspace_bytes() : best;
 }
 
 int w8a8_plan(int M, int K, int N, int blocks, w8a8_plan_t* plan) {
   if (!plan) return W8A8_ERR_INVALID_ARG;
-  GemmPlan pl;
-  int rc = gemm_plan(M, K, N, blocks, current_sm_count(), &pl);
+  AnyPlan ap;
+  int rc = any_plan(M, K, N, blocks, current_sm_count(), &ap);
   if (rc != W8A8_OK) return rc;
+  if (ap.tc) {
+    const TcPlan& pl = ap.t;
+    plan->n8_tiles = pl.mma_n / 8;
+    plan->n_tiles = pl.n_tiles;
+    plan->k_blocks = pl.kb;
+    plan->slabs = pl.units;
+    plan->blocks = pl.blocks;
+    plan->threads = pl.threads;
+    plan->stage_slabs = pl.stage_units;
+    plan->stages = pl.stages;
+    plan->smem_bytes = pl.smem_bytes;
+    plan->workspace_bytes = pl.workspace_bytes;
+    plan->combine_pack_bits = 0;
+    plan->tile_rows = 128;
+    plan->tensor_memory = 1;
+    return W8A8_OK;
+  }
+  const GemmPlan& pl = ap.g;
   plan->n8_tiles = pl.nt8;
   plan->n_tiles = pl.n_tiles;
   plan->k_blocks = pl.kb;
@@ -163,23 +196,32 @@ int w8a8_plan(int M, int K, int N, int blocks, w8a8_plan_t* plan) {
   plan->smem_bytes = pl.smem_bytes;
   plan->workspace_bytes = pl.workspace_bytes;
   plan->combine_pack_bits = pl.pack_f;
+  plan->tile_rows = 64;
+  plan->tensor_memory = 0;
   return W8A8_OK;
 }
 
-int w8a8_split_bounds(int K, int N, int blocks, long long* bounds, int n_bounds) {
+int w8a8_split_bounds_m(int M, int K, int N, int blocks, long long* bounds, int n_bounds) {
   if (!bounds) return W8A8_ERR_INVALID_ARG;
-  GemmPlan pl;
-  int rc = gemm_plan(1, K, N, blocks, current_sm_count(), &pl);
+  AnyPlan ap;
+  int rc = any_plan(M, K, N, blocks, current_sm_count(), &ap);
   if (rc != W8A8_OK) return rc;
-  if (n_bounds != pl.blocks + 1) return W8A8_ERR_INVALID_ARG;
-  const GemmSplit sp = make_gemm_split(pl.n_tiles, pl.kb, pl.blocks);
-  for (int i = 0; i < pl.blocks; ++i) {
+  const int n_tiles = ap.tc ? ap.t.n_tiles : ap.g.n_tiles;
+  const int kb = ap.tc ? ap.t.kb : ap.g.kb;
+  const int g = ap.tc ? ap.t.blocks : ap.g.blocks;
+  if (n_bounds != g + 1) return W8A8_ERR_INVALID_ARG;
+  const GemmSplit sp = make_gemm_split(n_tiles, kb, g);
+  for (int i = 0; i < g; ++i) {
     int b0, b1;
     gemm_split_run(sp, i, &b0, &b1);
     bounds[i] = b0;
   }
-  bounds[pl.blocks] = pl.slabs;
+  bounds[g] = (long long)n_tiles * kb;
   return W8A8_OK;
+}
+
+int w8a8_split_bounds(int K, int N, int blocks, long long* bounds, int n_bounds) {
+  return w8a8_split_bounds_m(1, K, N, blocks, bounds, n_bounds);
 }
 
 int w8a8_pack_weights(const int8_t* W, int K, int N, void* W_packed, void* ws, size_t ws_bytes, void* stream) {
@@ -200,15 +242,15 @@ int w8a8_gemm(const int8_t* x_q, const float* x_scale, const void* W_packed, con
               int M, int K, int N, int blocks, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
   if (!x_q || !x_scale || !W_packed || !w_scale || !out || !ws) return W8A8_ERR_INVALID_ARG;
   if (flags & ~(unsigned)W8A8_FLAG_PDL) return W8A8_ERR_INVALID_ARG;
-  GemmPlan pl;
-  int rc = gemm_plan(M, K, N, blocks, current_sm_count(), &pl);
+  AnyPlan pl;
+  int rc = any_plan(M, K, N, blocks, current_sm_count(), &pl);
   if (rc != W8A8_OK) return rc;
   if (!aligned(x_q, 16) || !aligned(W_packed, 16) || !aligned(out, 16) || !aligned(x_scale, 4) ||
       !aligned(w_scale, 4) || !aligned(ws, 256))
     return W8A8_ERR_MISALIGNED;
-  if (ws_bytes < pl.workspace_bytes) return W8A8_ERR_WORKSPACE_TOO_SMALL;
-  cudaError_t e = gemm_launch(pl, x_q, x_scale, W_packed, w_scale, out, M, K, N, ws, (flags & W8A8_FLAG_PDL) != 0,
-                              static_cast<cudaStream_t>(stream));
+  if (ws_bytes < pl.workspace_bytes()) return W8A8_ERR_WORKSPACE_TOO_SMALL;
+  cudaError_t e = any_launch(pl, x_q, x_scale, W_packed, w_scale, out, M, K, N, ws, (flags & W8A8_FLAG_PDL) != 0,
+                             static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "w8a8_gemm");
   return W8A8_OK;
 }

@@ -22,6 +22,37 @@ struct GemmPlan {
 int gemm_plan(int M, int K, int N, int blocks, int sm_count, GemmPlan* plan);
 cudaError_t gemm_launch(const GemmPlan& pl, const int8_t* x, const float* xs, const void* wp, const float* wsc,
                         void* out, int M, int K, int N, void* ws, bool pdl, cudaStream_t stream);
+
+// M ranges of the two W8A8 arms: the register-fed decode kernel up to kDecodeMaxM rows, the
+// tensor-memory (tcgen05) kernel above it up to kTcMaxM.
+constexpr int kDecodeMaxM = 32;
+constexpr int kTcMaxM = 128;
+
+struct TcPlan {
+  int mma_n;          // MMA N: activation rows covered (64 or 128)
+  int tiles64;        // 64-row packed tiles of N
+  int n_tiles;        // 128-row CTA tiles (pairs of packed tiles)
+  int kb;             // K / 32
+  long long units;    // n_tiles * kb: 32-k units of one CTA tile (the split's unit)
+  int blocks, threads, stage_units, stages;
+  size_t smem_bytes, workspace_bytes, counters_offset, partials_offset;
+};
+
+int tc_plan(int M, int K, int N, int blocks, int sm_count, TcPlan* plan);
+cudaError_t tc_launch(const TcPlan& pl, const int8_t* x, const float* xs, const void* wp, const float* wsc, void* out,
+                      int M, int K, int N, void* ws, bool pdl, cudaStream_t stream);
+
+// Either arm, chosen by M.
+struct AnyPlan {
+  bool tc;
+  GemmPlan g;
+  TcPlan t;
+  size_t workspace_bytes() const { return tc ? t.workspace_bytes : g.workspace_bytes; }
+};
+
+int any_plan(int M, int K, int N, int blocks, int sm_count, AnyPlan* plan);
+cudaError_t any_launch(const AnyPlan& pl, const int8_t* x, const float* xs, const void* wp, const float* wsc, void* out,
+                       int M, int K, int N, void* ws, bool pdl, cudaStream_t stream);
 cudaError_t pack_launch(const int8_t* W, int K, int N, void* out, cudaStream_t stream);
 
 struct Q8Plan {

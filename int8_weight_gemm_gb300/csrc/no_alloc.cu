@@ -1,4 +1,4 @@
-// w8a8_gemm_no_alloc: the W8A8 decode GEMM for callers that cannot allocate device memory.
+// w8a8_gemm_no_alloc: the W8A8 GEMM for callers that cannot allocate device memory.
 //
 // w8a8_gemm needs a caller-provided workspace (the split-tile accumulators).  Some callers have no way to provide one.  An inference plugin hosted inside
 // another engine sees only the input and output pointers the host engine hands it, with no access
@@ -58,14 +58,14 @@ extern "C" int w8a8_gemm_no_alloc(const int8_t* x_q, const float* x_scale, const
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
   }
   cudaGetLastError();
-  GemmPlan pl;
-  const int rc = gemm_plan(M, K, N, blocks, sms, &pl);
+  AnyPlan pl;
+  const int rc = any_plan(M, K, N, blocks, sms, &pl);
   if (rc != W8A8_OK) return rc;
   auto misaligned = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; };
   if (misaligned(x_q, 16) || misaligned(W_packed, 16) || misaligned(out, 16) || misaligned(x_scale, 4) ||
       misaligned(w_scale, 4))
     return W8A8_ERR_MISALIGNED;
-  if (pl.workspace_bytes > kNoAllocScratchBytes) {
+  if (pl.workspace_bytes() > kNoAllocScratchBytes) {
     record_error("w8a8_gemm_no_alloc: this shape needs more scratch than the built-in 16 MiB area");
     return W8A8_ERR_WORKSPACE_TOO_SMALL;
   }
@@ -75,9 +75,9 @@ extern "C" int w8a8_gemm_no_alloc(const int8_t* x_q, const float* x_scale, const
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The area keeps whatever the previous call left there: clear the part this call relies on
   // (status word and split-tile accumulators) before the kernel reads it.
-  e = cudaMemsetAsync(ws, 0, pl.workspace_bytes, s);
+  e = cudaMemsetAsync(ws, 0, pl.workspace_bytes(), s);
   if (e != cudaSuccess) return record_cuda_error(e, "w8a8_gemm_no_alloc (scratch clear)");
-  e = gemm_launch(pl, x_q, x_scale, W_packed, w_scale, out, M, K, N, ws, (flags & W8A8_FLAG_PDL) != 0, s);
+  e = any_launch(pl, x_q, x_scale, W_packed, w_scale, out, M, K, N, ws, (flags & W8A8_FLAG_PDL) != 0, s);
   if (e != cudaSuccess) return record_cuda_error(e, "w8a8_gemm_no_alloc");
   return W8A8_OK;
 }

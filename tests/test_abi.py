@@ -126,6 +126,77 @@ def test_plan_shape_and_limits():
     assert all(lib8.w8a8_plan(M, 4096, 1536)["workspace_bytes"] <= big for M in range(1, 33))
 
 
+def test_tensor_memory_arm_plan():
+    # 32 < M <= 128: 128-row tiles (two packed tiles), one CTA per SM, MMA N = 64 or 128.
+    p = lib8.w8a8_plan(128, 4096, 1536)
+    assert p["tensor_memory"] == 1 and p["tile_rows"] == 128 and p["n8_tiles"] == 16
+    assert p["n_tiles"] == 12 and p["k_blocks"] == 128 and p["slabs"] == 12 * 128
+    assert p["blocks"] == 152 and p["threads"] == 320 and p["smem_bytes"] <= 227 * 1024
+    q = lib8.w8a8_plan(33, 4096, 320)
+    assert q["n8_tiles"] == 8 and q["n_tiles"] == 3 and q["threads"] == 352
+    assert lib8.w8a8_plan(32, 4096, 320)["tensor_memory"] == 0
+    # header, counters (one per tile, padded to 256 bytes), int32 planes [tile][mma_n][128]
+    assert p["workspace_bytes"] == 256 + 256 + 12 * 128 * 128 * 4
+    assert q["workspace_bytes"] == 256 + 256 + 3 * 64 * 128 * 4
+    # the size query for M_max covers both arms
+    big = lib8.w8a8_workspace_bytes(128, 4096, 1536)
+    assert all(lib8.w8a8_plan(M, 4096, 1536)["workspace_bytes"] <= big for M in range(1, 129))
+    assert lib8.w8a8_workspace_bytes(129, 4096, 1536) == 0
+
+
+@pytest.mark.parametrize("M,K,N,blocks", [(64, 4096, 1536, 0), (128, 4096, 24576, 0), (100, 2048, 384, 7),
+                                          (33, 4000, 320, 0), (128, 32, 8, 1), (65, 12288, 4096, 304)])
+def test_tensor_memory_arm_split_bounds(M, K, N, blocks):
+    plan = lib8.w8a8_plan(M, K, N, blocks)
+    G, U, KB, T = plan["blocks"], plan["slabs"], plan["k_blocks"], plan["n_tiles"]
+    assert T == -(-N // 128) and U == T * KB
+    b = np.array(lib8.w8a8_split_bounds(K, N, G, M=M))
+    assert b[0] == 0 and b[-1] == U and len(b) == G + 1 and (np.diff(b) >= 1).all()
+    if G >= T:
+        assert all(b0 // KB == (b1 - 1) // KB for b0, b1 in zip(b[:-1], b[1:]))
+
+
+def test_tensor_memory_arm_row_assembly_emulated():
+    # CPU replay of the converter's index arithmetic: for every tensor-memory lane (tile row) the
+    # two 16-byte chunk reads, the exchange with lane ^ 8 and the selects must yield that row's 32
+    # weights of a 32-k unit in k order, from the packed layout the oracle writes.
+    K, N = 64, 128
+    W = synth.uniform_int8(5, "tc.W", (K, N), lo=-128, hi=127)
+    packed = oracle.w8a8_pack(W).astype(np.int64)
+    KB = K // 32
+
+    def words(off):
+        return [int(packed[off + 4 * i]) | int(packed[off + 4 * i + 1]) << 8 |
+                int(packed[off + 4 * i + 2]) << 16 | int(packed[off + 4 * i + 3]) << 24 for i in range(4)]
+
+    for quad in range(4):
+        half = quad >> 1
+        for unit in range(KB):
+            st = []
+            for lane in range(32):
+                s16, g = 2 * (quad & 1) + (lane >> 4), lane & 7
+                jr, bsw = (lane >> 3) & 1, (g >> 1) & 1
+                base = (half * KB + unit) * 2048
+                u = words(base + (s16 * 32 + 4 * g + 2 * jr + bsw) * 16)
+                v = words(base + (s16 * 32 + 4 * g + 2 * jr + 1 - bsw) * 16)
+                own = [(u[1], u[3]) if jr else (u[0], u[2]), (v[1], v[3]) if jr else (v[0], v[2])]
+                other = [(u[0], u[2]) if jr else (u[1], u[3]), (v[0], v[2]) if jr else (v[1], v[3])]
+                st.append((jr, bsw, own, other))
+            for lane in range(32):
+                jr, bsw, own, _ = st[lane]
+                ra, rb = st[lane ^ 8][3]
+                e = [own[1], own[0]] if bsw else own
+                f = [rb, ra] if bsw else [ra, rb]
+                chunks = f + e if jr else e + f
+                vals = []
+                for lo, hi in chunks:
+                    for w in (lo, hi):
+                        vals += [(((w >> (8 * i)) & 0xFF) ^ 0x80) - 256 * ((((w >> (8 * i)) & 0xFF) ^ 0x80) >= 128)
+                                 for i in range(4)]
+                row = 32 * quad + lane
+                assert vals == W[32 * unit:32 * unit + 32, row].tolist()
+
+
 def test_two_element_combine_words():
     # Field width from K (partial sums of an element are at most K * 2^14 in magnitude) and the
     # arrival count in the remaining bits; one element per word when the count would not fit.
@@ -169,7 +240,8 @@ def test_two_element_word_arithmetic():
 
 
 @pytest.mark.parametrize("M,K,N,blocks,code", [
-    (0, 512, 256, 0, 1), (33, 512, 256, 0, 1), (1, 0, 256, 0, 1), (1, 512, 0, 0, 1),
+    (0, 512, 256, 0, 1), (129, 512, 256, 0, 1), (1, 0, 256, 0, 1), (1, 512, 0, 0, 1),
+    (64, 500, 256, 0, 2), (64, 512, 250, 0, 2), (64, 512, 256, 10**6, 1),
     (1, 500, 256, 0, 2), (1, 512, 250, 0, 2), (1, 512, 256, -1, 1), (1, 512, 256, 10**6, 1)])
 def test_plan_rejects_bad_shapes(M, K, N, blocks, code):
     p = lib8.PlanT()
