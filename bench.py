@@ -248,7 +248,8 @@ def time_gemm(M, K, N, dist, seed, steps, warmup, blocks=0, device=None, sample_
     plan = lib8.w8a8_plan(M, K, N, blocks)
     res = {
         "R": R, "C": C, "wbytes": wbytes, "total_ms": total_ms, "steps": steps,
-        "kernel": f"w8a8_gemm_kernel<{plan['n8_tiles']}, {plan['stages']}, {str(plan['threads'] == 320).lower()}>",
+        "kernel": (f"w8a8_gemm_tc_kernel<{plan['n8_tiles'] // 2}>" if plan["tensor_memory"] else
+                   f"w8a8_gemm_kernel<{plan['n8_tiles']}, {plan['stages']}, {str(plan['threads'] == 320).lower()}>"),
         "blocks": plan["blocks"],
         "us_median": statistics.median(per_call_us),
         "us_p90": per_call_us[min(len(per_call_us) - 1, int(0.9 * len(per_call_us)))],
@@ -591,6 +592,10 @@ def run_sweep(args):
     shapes = [(1, 512, 256, "uniform", 0), (16, 4096, 1536, "uniform", 1)]
     shapes += [(M, K, N, "uniform", 3000 + M) for (N, K) in ((2560, 4096), (4096, 2048)) for M in (1, 4, 8, 16, 32)]
     shapes += [(16, 4096, 24576, "mlp", 4), (16, 12288, 4096, "mlp", 4)]
+    # 32 < M <= 128: the tensor-memory arm on the same weight shapes
+    shapes += [(M, K, N, "uniform", 5000 + M) for (N, K) in ((1536, 4096), (2560, 4096), (4096, 2048))
+               for M in (64, 128)]
+    shapes += [(128, 4096, 24576, "mlp", 5), (128, 12288, 4096, "mlp", 5), (48, 4096, 1536, "uniform", 5048)]
     if args.shapes:
         shapes = [shapes[int(i)] for i in args.shapes.split(",")]
     peak, _ = _peaks()
@@ -605,7 +610,8 @@ def run_sweep(args):
             r = time_gemm(M, K, N, dist, seed, args.steps, args.warmup, blocks=blocks, want_e2e=False, flags=flags)
             gbs = r["wbytes"] / (r["us_median"] * 1e-6) / 1e9
             row = {"M": M, "K": K, "N": N, "dist": dist, "blocks": blocks or lib8.w8a8_plan(M, K, N)["blocks"],
-                   "flags": flags,
+                   "flags": flags, "kernel": r["kernel"],
+                   "tflops": round(2.0 * M * N * K / (r["us_median"] * 1e-6) / 1e12, 1),
                    "us_median": round(r["us_median"], 3), "us_p90": round(r["us_p90"], 3),
                    "weight_GBps": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 3), "R": r["R"]}
             rows.append(row)
@@ -628,6 +634,8 @@ def run_ncu_driver(args):
 
     cfg = DEFAULT
     M, K, N = cfg["M"], cfg["K"], cfg["N"]
+    if args.ncu_shape:
+        M, K, N = (int(v) for v in args.ncu_shape.split(","))
     x, xs, W, ws = synth.w8a8_inputs(M, K, N, seed=cfg["seed"], dist=cfg["dist"])
     dev = torch.device("cuda")
     xd, xsd, wsd = (torch.from_numpy(a).to(dev) for a in (x, xs, ws))
@@ -656,6 +664,7 @@ def main():
     ap.add_argument("--shapes", default="", help="comma list of sweep shape indices (default: all)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-q8", action="store_true", help="skip the Q8_0 timings")
+    ap.add_argument("--ncu-shape", default="", help="M,K,N for --ncu-driver (default: the headline shape)")
     ap.add_argument("--ncu-driver", type=int, default=0,
                     help="profiling driver: this many eager calls of the default workload, then exit")
     args = ap.parse_args()

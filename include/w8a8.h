@@ -20,12 +20,14 @@
  *    caller owns every buffer.  `stream` is a cudaStream_t passed as void* (NULL = legacy stream).
  *  - Every argument check happens on the host before any launch.  A failed check launches
  *    nothing and returns a non-zero status; nothing is thrown and nothing is printed.
- *  - w8a8_gemm and q8_0_gemv do no host synchronisation, allocation or memset: each is exactly
- *    one kernel launch, so a call can be captured into a CUDA graph and replayed.
+ *  - w8a8_gemm and q8_0_gemv do no host synchronisation, allocation or memset, so a call can be
+ *    captured into a CUDA graph and replayed.  Each is one kernel launch, except w8a8_gemm with
+ *    M > 32: two launches (the activations converted to fp16 into the workspace, then the GEMM
+ *    as a programmatic dependent of that launch).
  *  - A workspace is caller-owned device memory, at least 256-byte aligned, sized with the
  *    *_workspace_bytes queries and zeroed once with w8a8_workspace_init (outside any capture)
  *    before its first use.  Every call leaves it ready for the next one (each arrival counter is
- *    reset by the last arrival).  Calls that use the same workspace must not overlap in time
+ *    reset by the last arrival, and every accumulator returned to zero).  Calls that use the same workspace must not overlap in time
  *    (use one stream per workspace); one workspace may serve both operators in turn if it is
  *    sized for the larger of the two.
  *  - bf16 and fp16 values are passed as their 16-bit patterns (uint16_t storage).
@@ -105,9 +107,11 @@ size_t w8a8_packed_weight_bytes(int K, int N);
 /* Workspace bytes that w8a8_gemm needs for every M in [1, M_max] (M_max <= 128) at this (K, N)
  * and `blocks` (0 = the automatic plan, whose CTA count follows the current device's SM count).
  * Returns 0 for arguments w8a8_gemm would reject.  Layout: a 256-byte header (status word first),
- * then, for M <= 32, one 64-bit accumulator word per output element of every 64-row tile; for
- * M > 32, one 32-bit arrival counter per 128-row tile (padded to 256 bytes) and one int32 sum
- * per (tile, activation row < 64 or 128, tile row).  All of it is zero between calls. */
+ * then, for M <= 32, one 64-bit accumulator word per output element of every 64-row tile (zero
+ * between calls); for M > 32, one 32-bit arrival counter per 128-row tile (padded to 256 bytes)
+ * and one int32 sum per (tile, activation row < 128, tile row), both zero between calls, then the
+ * call's activations as fp16 [M][K] (overwritten by every call).  The regions sit at offsets that
+ * do not depend on M, so calls of any M in [1, M_max] may share one workspace in turn. */
 size_t w8a8_workspace_bytes(int M_max, int K, int N, int blocks);
 
 /* Pack W once, at load time and outside any timed region or capture (section 1.1 of the W8A8

@@ -35,7 +35,7 @@ struct TcPlan {
   int kb;             // K / 32
   long long units;    // n_tiles * kb: 32-k units of one CTA tile (the split's unit)
   int blocks, threads, stage_units, stages;
-  size_t smem_bytes, workspace_bytes, counters_offset, partials_offset;
+  size_t smem_bytes, workspace_bytes, counters_offset, partials_offset, x16_offset;
 };
 
 int tc_plan(int M, int K, int N, int blocks, int sm_count, TcPlan* plan);

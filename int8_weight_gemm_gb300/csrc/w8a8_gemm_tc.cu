@@ -7,7 +7,7 @@
 // the same (K, N): the decode pattern does not carry over once M grows.  This file is that arm.
 // Split-K and the last-arrival combine follow the page's section 1.1 (qkv recipe): monotonic
 // work split over the SM count, per-tile arrival counters in the workspace, the last arriver sums
-// the partials, scales them and stores bf16, and every call leaves the workspace zeroed.
+// the partials, scales them and stores bf16, and every call leaves the counters and sums zeroed.
 //
 // Why tcgen05 here.  With M activation rows, every weight byte feeds 2M multiply-adds; at M = 128
 // a weight stream at HBM speed needs ~1.8 PFLOP/s, three times what the register-fed mma.sync path
@@ -17,23 +17,31 @@
 // is an fp16 integer) and multiplied with kind::f16.
 //
 // Exactness.  A product is an integer of magnitude <= 2^14; one accumulator collects at most
-// 512 k (four stages) before the epilogue warps read it out, so every f32 accumulator value is an
-// integer of magnitude <= 2^23 and exact.  The read-out converts it to int32 (exact) and adds it
-// to int32 sums; split tiles add int32 partials.  The result is the int32 sum an int8 MMA would
-// give, bit for bit, whatever the split.
+// 512 k (four stages) before it is read out, so every f32 accumulator value is an integer of
+// magnitude <= 2^23 and exact.  The read-out converts it to int32 (exact) and adds it to int32
+// sums; split tiles add int32 partials.  The result is the int32 sum an int8 MMA would give, bit
+// for bit, whatever the split.
 //
-// Roles (one CTA per SM, all of its tensor memory):
-//  * producer (one thread): per stage of 128 k, two 1-D bulk copies of packed weight (the CTA's
-//    128-row tile is two consecutive 64-row packed tiles) and one 2-D tensor-map box of
-//    activations (128 bytes x N_mma rows, 128-byte swizzle, zero fill past M and K) into a ring;
-//  * eight converter warps: the weight rows go into tensor memory as the fp16 A operand
-//    (tcgen05.st, lane = row), the activations into shared memory as the fp16 B operand
-//    (K-major, no swizzle).  The same warps retire each stage once its MMAs have completed (they
-//    wait for that anyway before reusing its operand slot): at the end of a period they read the
-//    accumulators out and keep int32 sums in registers (each warp one lane quarter and one half
-//    of the columns), and at the end of a segment they store bf16 or add the split tile's
-//    partial and, as the last arrival, finish it;
-//  * one or two MMA-issuing threads (each takes every other k-step into its own accumulators).
+// One call is two launches:
+//  * x16: the activations converted once to fp16 (exact) into the workspace, in the k order the
+//    converted weight has in tensor memory, so that no CTA converts them again; it lets the GEMM
+//    launch at once (programmatic dependent launch);
+//  * the GEMM (one CTA per SM, all of its tensor memory), launched as a programmatic dependent of
+//    x16: its weight stream starts while x16 runs.  Roles:
+//    - weight producer (one thread): per stage of 128 k, two 1-D bulk copies of packed weight (the
+//      CTA's 128-row tile is two consecutive 64-row packed tiles) into a deep ring that the
+//      converter warps free as soon as they have read a stage, so it holds the bytes in flight
+//      from HBM;
+//    - activation producer (one thread): per stage two 2-D tensor-map boxes of fp16 activations
+//      (64 k x N_mma rows each, 128-byte swizzle: the MMA's B operand as it lands) into a short
+//      ring that the MMAs free;
+//    - sixteen converter warps: the weight rows go into tensor memory as the fp16 A operand
+//      (tcgen05.st, lane = row, one packed 16-byte chunk per thread and store).  The same warps retire each stage once its MMAs have completed
+//      (they wait for that anyway before reusing its tensor-memory slot): at the end of a period
+//      they read the accumulators out and keep int32 sums in registers (each warp one lane
+//      quarter and one quarter of the columns), and at the end of a segment they store bf16 or
+//      add the split tile's partial and, as the last arrival, finish it;
+//    - one or two MMA-issuing threads (two take alternate k-steps into their own accumulators).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -49,41 +57,45 @@ constexpr int kKBlock = 32;                          // k per unit of the split
 constexpr int kPackSlab = kPackRows * kKBlock;       // 2048: one packed slab
 constexpr int kStageUnits = 4;                       // 32-k units per stage
 constexpr int kStageK = kStageUnits * kKBlock;       // 128
+constexpr int kBoxK = 64;                            // k of one activation box (128 bytes of fp16)
 constexpr int kHalfBytes = kStageUnits * kPackSlab;  // one packed tile's share of a stage: 8 KiB
 constexpr int kWStage = 2 * kHalfBytes;              // 16 KiB of weight per stage
-constexpr int kConvWarps = 8;                        // two per tensor-memory lane quarter
+constexpr int kConvWarps = 16;                       // four per tensor-memory lane quarter
 constexpr int kConvThreads = 32 * kConvWarps;
-constexpr int kProducerWarp = kConvWarps;
-constexpr int kMmaWarp = kProducerWarp + 1;          // first MMA-issuing warp; owns tensor memory
+constexpr int kWProducerWarp = kConvWarps;           // streams the packed weight
+constexpr int kBProducerWarp = kConvWarps + 1;       // loads the activation boxes
+constexpr int kMmaWarp = kConvWarps + 2;             // first MMA-issuing warp; owns tensor memory
 constexpr int kPeriodStages = 4;                     // stages per accumulator read-out (512 k)
 constexpr int kTmemCols = 512;
 constexpr int kACols = kStageK / 2;                  // tensor-memory columns of one A stage (fp16 pairs)
-constexpr int kBSbo = (kStageK / 8) * 128;           // B operand: bytes between 8-row groups
 constexpr int kConvBarrier = 1;                      // named barrier of the converter warps
 
 template <int NT16>
 struct TcLayout {
   static constexpr int kN = 16 * NT16;               // MMA N: activation rows (zero past M)
-  // An MMA at N = 64 is short next to an issuing thread's per-instruction cost, so two threads
-  // issue; at N = 128 one keeps the tensor core busy and the accumulators fill tensor memory.
+  // The issue cost of an MMA is per instruction, so the widest MMA (N = kN) is the cheapest.  At
+  // N = 64 two threads issue, each every other k-step of a stage into its own accumulators (the
+  // read-out adds them); at N = 128 the accumulators of a second thread would not fit next to the A
+  // ring, and one thread issues.  (Splitting the activation rows between two threads instead gives
+  // each the same number of MMAs and was measured to gain nothing.)
   static constexpr int kIssuers = kN <= 64 ? 2 : 1;
-  static constexpr int kRawStages = kN <= 64 ? 6 : 4;
-  static constexpr int kOpStages = kN <= 64 ? 4 : 3;
-  static constexpr int kXBox = kN * 128;              // raw activation box, 1 KiB multiple
-  static constexpr int kRaw = kXBox + kWStage;        // one raw stage (box first: 1 KiB aligned)
-  static constexpr int kBStage = kN * kStageK * 2;    // fp16 B operand of one stage
+  // The weight ring is freed as soon as the converter warps have read a stage, so it can be deep:
+  // it holds the bytes in flight from HBM.  The activation ring (from L2) is freed by the MMAs.
+  static constexpr int kWStages = kN <= 64 ? 10 : 8;
+  static constexpr int kBStages = kN <= 64 ? 4 : 3;
+  static constexpr int kOpStages = kN <= 64 ? 4 : 3;  // tensor-memory ring of converted weight
+  static constexpr int kBBox = kN * 128;              // one fp16 activation box (1 KiB multiple)
+  static constexpr int kBStage = 2 * kBBox;
   static constexpr int kDCol0 = kOpStages * kACols;   // first accumulator column
   static constexpr int kThreads = 32 * (kMmaWarp + kIssuers);
-  static constexpr int kBytes = 1024 + kRawStages * kRaw + kOpStages * kBStage;
-  static constexpr int kXPieces = kN * (kStageK / 16) / (32 * kConvWarps);   // 16-byte pieces per thread
-  static constexpr int kCols = kN / 2;                // accumulator columns per converter warp
+  static constexpr int kBytes = 1024 + kBStages * kBStage + kWStages * kWStage;   // boxes first: 1 KiB aligned
+  static constexpr int kCols = kN / 4;                // accumulator columns per converter warp
   static_assert(kDCol0 + kIssuers * 2 * kN <= kTmemCols, "tensor-memory columns");
   static_assert(kBytes <= 232448 - 2048, "shared memory");
-  static_assert(kXPieces * 32 * kConvWarps == kN * (kStageK / 16), "activation pieces");
 };
 
 struct TcParams {
-  CUtensorMap xmap;     // x_q [M,K] int8, box 128 bytes x N_mma rows, 128-byte swizzle
+  CUtensorMap xmap;     // fp16 activations [M,K] in the workspace, box 64 x N_mma, 128-byte swizzle
   const uint8_t* wp;    // packed weight (64-row tiles of 2 KiB slabs)
   const float* x_scale;
   const float* w_scale;
@@ -93,7 +105,6 @@ struct TcParams {
   int* planes;          // [tile][m < N_mma][row < 128] int32 sums of a split tile, zero between calls
   GemmSplit split;      // over the 128-row tiles, in 32-k units
   int M, N, KB, tiles64;
-  int pdl;
 };
 
 // The CTA's schedule: its run of units [b0, b1) is a sequence of segments (one tile's part each),
@@ -141,6 +152,17 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
                : "memory");
 }
 
+// Shared-memory matrix descriptor, K-major with the 128-byte swizzle: rows of 128 bytes (64 fp16
+// of k), 16-byte chunks XOR-ed with the row index mod 8, atoms of 8 rows 1024 bytes apart (the
+// stride field), the leading-dimension field unused (1).  Layout type 2 in bits 61..63, descriptor
+// version 1 in bits 46..47, base offset 0 (atoms 1024-byte aligned).  Within an atom the k-steps
+// of 16 start 32 bytes apart: the swizzle applies to the address bits, so the start moves by the
+// unswizzled offset.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
 // int32 load that bypasses L1 (the partial sums of other CTAs).
 __device__ __forceinline__ int ld_relaxed_s32(const int* p) {
   int v;
@@ -156,19 +178,97 @@ __device__ __forceinline__ uint16_t epilogue(int acc, float xsv, float wsv) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
+// Bounded wait for the phase of `parity` that polls with the non-blocking mbarrier.test_wait.  Every
+// role of this kernel blocks on a barrier once or more per stage, and a thread suspended in
+// mbarrier.try_wait was measured to resume well after the phase completes, so these waits spin.
+// Gives up when another thread has raised *abort, or after kWaitTimeoutCycles (then records the
+// timeout in *status and raises *abort).  Returns true when the phase completed.
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* status) {
+  const long long t0 = clock64();
+  for (int n = 0;; ++n) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((n & 63) == 63) {
+      if (*abort) return false;
+      if (clock64() - t0 > kWaitTimeoutCycles) {
+        atomicOr(status, W8A8_DEV_WAIT_TIMEOUT);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // mbar_wait taken by a whole warp: the warp goes on only if every lane saw the phase complete, so
 // the warp-wide tensor-memory instructions after it always run with all 32 lanes.
 __device__ __forceinline__ bool mbar_wait_all(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* status) {
-  const bool ok = mbar_wait(bar, parity, abort, status);
+  const bool ok = tc_wait(bar, parity, abort, status);
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
-// Bounded wait of all converter threads on one phase of `bar` (count kConvThreads).
-__device__ __forceinline__ bool epi_sync(uint64_t* bar, uint32_t& phase, volatile int* abort, uint32_t* status) {
-  mbar_arrive(bar);
-  const bool ok = mbar_wait_all(bar, phase, abort, status);
+// Bounded wait on one phase of `bar` for a whole warp: lane 0 polls, the other lanes wait for it at
+// the warp barrier of the broadcast; the outcome is the same for all 32 lanes.  For waits whose next
+// step is a tensor-memory instruction behind tcgen05.fence::after_thread_sync.
+__device__ __forceinline__ bool mbar_wait_lane0(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* status) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = tc_wait(bar, parity, abort, status) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// One arrival for the warp, after every lane's earlier work (the warp barrier orders it).  Barriers
+// the converter warps signal count warps, not threads: 512 arrivals on one shared-memory word per
+// stage were measured to cost more than the stage's work.
+__device__ __forceinline__ void mbar_arrive_warp(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+// Bounded meeting of all converter warps on one phase of `bar` (count kConvWarps).
+__device__ __forceinline__ bool conv_sync(uint64_t* bar, uint32_t& phase, volatile int* abort, uint32_t* status) {
+  mbar_arrive_warp(bar);
+  const bool ok = mbar_wait_lane0(bar, phase, abort, status);
   phase ^= 1u;
   return ok;
+}
+
+// The weight's k order inside tensor memory.  A converter thread writes one packed 16-byte chunk
+// (rows g and g + 8 of a 16-row group, k = 8c ... 8c + 7 of a 32-k unit) with the 16x256b shape, so
+// tensor-memory column j of the unit (the MMA's k pair 2j, 2j + 1) holds the weight pair
+// k = 8 ((j % 8) / 2) + 2 ((j % 2) + 2 (j / 8)) + {0, 1}.  In groups of four k: the MMA's groups
+// 0 ... 7 of a unit are the weight's groups 0, 2, 4, 6, 1, 3, 5, 7.  The activations are written in
+// the same order, so every product pairs the same k on both sides and the dot product is the
+// plain sum over k.
+
+// int8 activations -> fp16 (exact) in the MMA's k order, one 32-k unit of one row per thread step.
+__global__ void __launch_bounds__(256) x16_kernel(const uint4* __restrict__ x, uint4* __restrict__ x16, long long units) {
+  pdl_trigger();   // the GEMM may launch now: it streams weight until this grid has completed
+  pdl_wait();      // x_q may come from the previous grid, and the previous call may still read x16
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < units; i += stride) {
+    const uint4 a = __ldg(x + 2 * i), b = __ldg(x + 2 * i + 1);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t h[16];   // group gi of four k as fp16 pairs h[2 gi], h[2 gi + 1]
+#pragma unroll
+    for (int gi = 0; gi < 8; ++gi) offset_bytes_to_half2_pairs(w[gi] ^ 0x80808080u, h[2 * gi], h[2 * gi + 1]);
+    uint4* o = x16 + 4 * i;
+    o[0] = make_uint4(h[0], h[1], h[4], h[5]);      // groups 0, 2
+    o[1] = make_uint4(h[8], h[9], h[12], h[13]);    // groups 4, 6
+    o[2] = make_uint4(h[2], h[3], h[6], h[7]);      // groups 1, 3
+    o[3] = make_uint4(h[10], h[11], h[14], h[15]);  // groups 5, 7
+  }
+}
+
+// 16 lanes x 16 columns: thread t writes lanes t / 4 (v0, v1, v4, v5) and t / 4 + 8 (v2, v3, v6, v7),
+// columns 2 (t % 4), 2 (t % 4) + 1 (v0 ... v3) and the same plus 8 (v4 ... v7); warp-wide.
+__device__ __forceinline__ void tmem_st_16x256_x2(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.16x256b.x2.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
 }
 
 template <int NT16>
@@ -176,13 +276,16 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
   using L = TcLayout<NT16>;
   constexpr int kN = L::kN;
   constexpr int kI = L::kIssuers;
-  constexpr int NR = L::kRawStages;
+  constexpr int NW = L::kWStages;
+  constexpr int NB = L::kBStages;
   constexpr int NA = L::kOpStages;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[NR];    // a raw stage landed (weight halves + activation box)
-  __shared__ __align__(8) uint64_t empty_bar[NR];   // the converter warps have read a raw stage
-  __shared__ __align__(8) uint64_t conv_bar[NA];    // A (tensor memory) and B (shared memory) written
-  __shared__ __align__(8) uint64_t mma_bar[NA];     // the MMAs reading an operand stage completed
+  __shared__ __align__(8) uint64_t wfull_bar[NW];   // a weight stage landed
+  __shared__ __align__(8) uint64_t wempty_bar[NW];  // the converter warps have read a weight stage
+  __shared__ __align__(8) uint64_t bfull_bar[NB];   // an activation stage (two boxes) landed
+  __shared__ __align__(8) uint64_t bdone_bar[NB];   // the MMAs reading an activation stage completed
+  __shared__ __align__(8) uint64_t adone_bar[NA];   // the MMAs reading a tensor-memory A stage completed
+  __shared__ __align__(8) uint64_t conv_bar[NA];    // a tensor-memory A stage written (its activations landed)
   __shared__ __align__(8) uint64_t dempty_bar[2];   // an accumulator buffer has been read out
   __shared__ __align__(8) uint64_t final_bar[kI];   // every MMA of an issuer completed
   __shared__ __align__(8) uint64_t sync_bar;        // converter warps meet at a split tile's combine
@@ -191,28 +294,33 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
   __shared__ int abort_flag;
   __shared__ uint32_t last_flag;
 
-  uint8_t* const smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* const raw = smem;                        // NR x [activation box | weight half 0 | weight half 1]
-  uint8_t* const bring = smem + NR * L::kRaw;       // NA x fp16 B operand
+  // NB x [activation box k 0..63 | box k 64..127] (1 KiB aligned for the swizzle), then NW weight stages.
+  uint8_t* const bring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* const wring = bring + NB * L::kBStage;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
 #pragma unroll
-    for (int s = 0; s < NR; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], kConvWarps);
+    for (int s = 0; s < NW; ++s) {
+      mbar_init(&wfull_bar[s], 1);
+      mbar_init(&wempty_bar[s], kConvWarps);
+    }
+#pragma unroll
+    for (int s = 0; s < NB; ++s) {
+      mbar_init(&bfull_bar[s], 1);
+      mbar_init(&bdone_bar[s], kI);
     }
 #pragma unroll
     for (int a = 0; a < NA; ++a) {
-      mbar_init(&conv_bar[a], kConvThreads);
-      mbar_init(&mma_bar[a], kI);
+      mbar_init(&adone_bar[a], kI);
+      mbar_init(&conv_bar[a], kConvWarps);
     }
 #pragma unroll
-    for (int d = 0; d < 2; ++d) mbar_init(&dempty_bar[d], kConvThreads);
+    for (int d = 0; d < 2; ++d) mbar_init(&dempty_bar[d], kConvWarps);
 #pragma unroll
     for (int i = 0; i < kI; ++i) mbar_init(&final_bar[i], 1);
-    mbar_init(&sync_bar, kConvThreads);
+    mbar_init(&sync_bar, kConvWarps);
     abort_flag = 0;
     mbar_fence_init();
   }
@@ -220,54 +328,55 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  pdl_trigger();   // the next call on the stream may start its own weight prefetch
+  pdl_trigger();   // the next call on the stream may start its own launches
   const uint32_t tmem = tmem_base;
 
   int b0, b1;
   gemm_split_run(p.split, blockIdx.x, &b0, &b1);
 
-  if (warp == kProducerWarp) {
-    // ---------------------------------------------------------------- producer (one thread)
+  if (warp == kWProducerWarp) {
+    // ---------------------------------------------------------------- weight producer (one thread)
+    // The packed weight is never written by the work this grid depends on, so this thread never
+    // waits for it: the weight streams from the first cycle.
     if (lane == 0) {
-      tma_prefetch_desc(&p.xmap);
       const uint64_t policy = policy_evict_first();
-      // Weight halves of stage `w` into raw slot s; the expected bytes include the activation box.
-      auto issue_w = [&](int s, const Walk& w) {
-        const int t64 = 2 * w.t;
-        const bool two = t64 + 1 < p.tiles64;
-        const uint32_t bytes = (uint32_t)(w.ns * kPackSlab);
-        mbar_arrive_expect_tx(&full_bar[s], bytes * (two ? 2u : 1u) + (uint32_t)L::kXBox);
-        uint8_t* dst = raw + s * L::kRaw + L::kXBox;
-        const uint8_t* src = p.wp + ((size_t)t64 * p.KB + w.kb0()) * kPackSlab;
-        bulk_g2s_hint(dst, src, bytes, &full_bar[s], policy);
-        if (two) bulk_g2s_hint(dst + kHalfBytes, src + (size_t)p.KB * kPackSlab, bytes, &full_bar[s], policy);
-      };
-      auto issue_x = [&](int s, const Walk& w) {
-        tma_load_2d(raw + s * L::kRaw, &p.xmap, w.kb0() * kKBlock, 0, &full_bar[s]);
-      };
-      Walk it(b0, b1, p.KB);
       int q = 0;
-      if (p.pdl) {
-        // The packed weight is never written by the work this call depends on: stream it before the
-        // dependency wait, and add the activation boxes once the wait has returned.
-        Walk pre = it;
-        int npre = 0;
-        for (; npre < NR && !pre.done(); ++npre, pre.next()) issue_w(npre, pre);
-        pdl_wait();
-        for (; q < npre; ++q, it.next()) issue_x(q, it);
-      } else {
-        pdl_wait();
-      }
-      for (; !it.done(); it.next(), ++q) {
-        const int s = q % NR;
-        if (q >= NR && !mbar_wait(&empty_bar[s], (uint32_t)(((q / NR) & 1) ^ 1), &abort_flag, p.status)) break;
-        issue_w(s, it);
-        issue_x(s, it);
+      for (Walk it(b0, b1, p.KB); !it.done(); it.next(), ++q) {
+        const int s = q % NW;
+        if (q >= NW && !tc_wait(&wempty_bar[s], (uint32_t)(((q / NW) & 1) ^ 1), &abort_flag, p.status)) break;
+        const int t64 = 2 * it.t;
+        const bool two = t64 + 1 < p.tiles64;
+        const uint32_t bytes = (uint32_t)(it.ns * kPackSlab);
+        mbar_arrive_expect_tx(&wfull_bar[s], bytes * (two ? 2u : 1u));
+        uint8_t* dst = wring + s * kWStage;
+        const uint8_t* src = p.wp + ((size_t)t64 * p.KB + it.kb0()) * kPackSlab;
+        bulk_g2s_hint(dst, src, bytes, &wfull_bar[s], policy);
+        if (two) bulk_g2s_hint(dst + kHalfBytes, src + (size_t)p.KB * kPackSlab, bytes, &wfull_bar[s], policy);
       }
       // Every copy issued must land before the CTA may exit.
-      for (int s = 0; s < NR && s < q; ++s) {
-        const int last = s + NR * ((q - 1 - s) / NR);
-        mbar_wait_drain(&full_bar[s], (uint32_t)((last / NR) & 1), p.status);
+      for (int s = 0; s < NW && s < q; ++s) {
+        const int last = s + NW * ((q - 1 - s) / NW);
+        mbar_wait_drain(&wfull_bar[s], (uint32_t)((last / NW) & 1), p.status);
+      }
+    }
+  } else if (warp == kBProducerWarp) {
+    // ---------------------------------------------------------------- activation producer (one thread)
+    if (lane == 0) {
+      tma_prefetch_desc(&p.xmap);
+      pdl_wait();   // the fp16 activations are written by the grid this one depends on
+      int q = 0;
+      for (Walk it(b0, b1, p.KB); !it.done(); it.next(), ++q) {
+        const int s = q % NB;
+        // The slot is free once the MMAs of stage q - NB (which read it) have completed.
+        if (q >= NB && !tc_wait(&bdone_bar[s], (uint32_t)(((q - NB) / NB) & 1), &abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&bfull_bar[s], (uint32_t)L::kBStage);
+        const int k0 = it.kb0() * kKBlock;
+        tma_load_2d(bring + s * L::kBStage, &p.xmap, k0, 0, &bfull_bar[s]);
+        tma_load_2d(bring + s * L::kBStage + L::kBBox, &p.xmap, k0 + kBoxK, 0, &bfull_bar[s]);
+      }
+      for (int s = 0; s < NB && s < q; ++s) {
+        const int last = s + NB * ((q - 1 - s) / NB);
+        mbar_wait_drain(&bfull_bar[s], (uint32_t)((last / NB) & 1), p.status);
       }
     }
   } else if (warp >= kMmaWarp) {
@@ -277,28 +386,33 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
       constexpr uint32_t idesc = idesc_f16_f32(kTileRows, kN);
       bool started = false;   // this issuer's accumulator of the current period holds a k-step
       for (Walk it(b0, b1, p.KB); !it.done(); it.next()) {
+        const int sb = it.q % NB;
         const int a = it.q % NA;
         const int db = it.period & 1;
         if (it.period_first() && it.period >= 2 &&
-            !mbar_wait(&dempty_bar[db], (uint32_t)(((it.period >> 1) - 1) & 1), &abort_flag, p.status))
+            !tc_wait(&dempty_bar[db], (uint32_t)(((it.period >> 1) - 1) & 1), &abort_flag, p.status))
           break;
-        if (!mbar_wait(&conv_bar[a], (uint32_t)((it.q / NA) & 1), &abort_flag, p.status)) break;
+        // The converter warps saw the activation stage land before they finished the A stage: one
+        // wait covers both operands.
+        if (!tc_wait(&conv_bar[a], (uint32_t)((it.q / NA) & 1), &abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_addr = tmem + (uint32_t)(L::kDCol0 + (issuer * 2 + db) * kN);
         const uint32_t a_addr = tmem + (uint32_t)(a * kACols);
-        const uint32_t b_addr = smem_addr(bring + a * L::kBStage);
+        const uint32_t b_addr = smem_addr(bring + sb * L::kBStage);
         if (it.period_first()) started = false;
-        // k-step j covers k in [16 j, 16 j + 16) of the stage: A columns 8 j ... 8 j + 7, B core
-        // matrices 2 j and 2 j + 1 (128 bytes apart), 8-row groups kBSbo bytes apart.  Every issuer
-        // has at least one k-step per stage (a stage has 2 ns >= 2 of them).
+        // k-step j covers k in [16 j, 16 j + 16) of the stage: A columns 8 j ... 8 j + 7; B in box
+        // j / 4 at byte 32 (j % 4) of each 128-byte row.  Every issuer has at least one k-step per
+        // stage (a stage has 2 ns >= 2 of them).
         for (int j = issuer; j < 2 * it.ns; j += kI) {
-          umma_f16_tmem_a(d_addr, a_addr + 8u * j, smem_desc_kmajor(b_addr + 256u * j, 128u, (uint32_t)kBSbo), idesc,
-                          started);
+          const uint64_t bdesc = smem_desc_sw128(b_addr + (uint32_t)((j >> 2) * L::kBBox + (j & 3) * 32));
+          umma_f16_tmem_a(d_addr, a_addr + 8u * j, bdesc, idesc, started);
           started = true;
         }
-        // Completes once these MMAs (and every earlier one of this thread) have completed: frees the
-        // operand stage and, at a period's end, lets the converter warps read the accumulators.
-        umma_commit(&mma_bar[a]);
+        // Each completes once these MMAs (and every earlier one of this thread) have completed: the
+        // activation slot and the A stage are free again and, at a period's end, the converter warps
+        // may read the accumulators.
+        umma_commit(&bdone_bar[sb]);
+        umma_commit(&adone_bar[a]);
       }
       // Whatever happened above, every MMA this thread issued completes before tensor memory is freed.
       umma_commit(&final_bar[issuer]);
@@ -306,29 +420,20 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
     }
   } else {
     // ---------------------------------------------------------------- converter warps
-    // Warp w owns tensor-memory lanes 32 (w % 4) ... + 31 (rows of the CTA tile), units
-    // 2 (w / 4), 2 (w / 4) + 1 of every stage, and accumulator columns (w / 4) kN / 2 ... + kN / 2 - 1.
-    // Row r of the tile is row r % 64 = 16 s + g + 8 j of packed tile r / 64; a packed 16-byte
-    // chunk (s, 4 g + c) holds k = 8c ... 8c + 7 of rows g and g + 8 (words: row g k 8c.., row
-    // g + 8 k 8c.., row g k 8c+4.., row g + 8 k 8c+4..).  The two threads of rows g and g + 8
-    // (lanes L and L ^ 8) each read two of the four chunks of their pair, trade the other row's
-    // words, convert their own row's 32 values and write them as 16 fp16 pairs (tcgen05.st, columns
-    // in k order).  Chunk choice by bit 1 of g spreads a quarter warp's reads over four bank groups.
-    // The 256 converter threads also turn the stage's raw activation box into the fp16 B operand:
-    // element (m, k) at (m / 8) kBSbo + (k / 8) 128 + (m % 8) 16 + (k % 8) 2.
-    const int quad = warp & 3, upair = warp >> 2;
+    // Warp w owns tensor-memory lanes 32 (w % 4) ... + 31 (rows of the CTA tile), unit w / 4 of every
+    // stage, and accumulator columns (w / 4) kN / 4 ... + kN / 4 - 1.  Its 32 rows are two 16-row
+    // groups s of packed tile (w % 4) / 2; the packed 16-byte chunk (s, lane) holds k = 8c ... 8c + 7
+    // of rows g and g + 8 (g = lane / 4, c = lane % 4; words: row g k 8c.., row g + 8 k 8c.., row g
+    // k 8c+4.., row g + 8 k 8c+4..), which is what the 16x256b store takes from thread `lane`: one
+    // 16-byte read (a group is 512 contiguous bytes), four exact conversions, one store per group.
+    const int quad = warp & 3, unit = warp >> 2;
     const int half = quad >> 1;
-    const int s16 = 2 * (quad & 1) + (lane >> 4);
-    const int g = lane & 7;
-    const bool jr = ((lane >> 3) & 1) != 0;
-    const bool bsw = ((g >> 1) & 1) != 0;
-    const int cA = 2 * (int)jr + (int)bsw, cB = 2 * (int)jr + 1 - (int)bsw;
-    const int offA = (s16 * 32 + 4 * g + cA) * 16, offB = (s16 * 32 + 4 * g + cB) * 16;
+    const int s16 = 2 * (quad & 1);
     const uint32_t t_lane = tmem + ((uint32_t)(32 * quad) << 16);
     const int row = 32 * quad + lane;
-    const int m0 = upair * L::kCols;
+    const int m0 = unit * L::kCols;
 
-    pdl_wait();   // x_scale, w_scale, out and the workspace may belong to the previous call
+    pdl_wait();   // x_scale, w_scale, out and the workspace may belong to earlier work on the stream
     for (int i = threadIdx.x; i < kN; i += kConvThreads) xs_sm[i] = i < p.M ? __ldg(p.x_scale + i) : 0.f;
     named_bar_sync(kConvBarrier, kConvThreads);
 
@@ -359,11 +464,11 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
           }
         }
         tc_fence_before();
-        mbar_arrive(&dempty_bar[db]);
+        mbar_arrive_warp(&dempty_bar[db]);
         if (dr.seg_last()) {
           // Element (m0 + c, n) of out, walked down the column one activation row at a time.
           uint16_t* o = p.out + (size_t)m0 * p.N + n;
-          const int mrows = min(L::kCols, p.M - m0);   // rows of this thread's half that exist
+          const int mrows = min(L::kCols, p.M - m0);   // rows of this warp's columns that exist
           if (dr.whole_tile()) {
             if (n < p.N) {
 #pragma unroll
@@ -380,7 +485,7 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
                 if (c < mrows) red_add_s32(plane + c * kTileRows, iacc[c]);
             }
             __threadfence();
-            if (!epi_sync(&sync_bar, sync_phase, &abort_flag, p.status)) return false;
+            if (!conv_sync(&sync_bar, sync_phase, &abort_flag, p.status)) return false;
             if (threadIdx.x == 0) {
               const uint32_t arrivals = (uint32_t)gemm_split_contributors(p.split, dr.t);
               const uint32_t old = atom_add_acq_rel_u32(p.counters + dr.t, 1u);
@@ -389,7 +494,7 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
               if (last) p.counters[dr.t] = 0u;   // every contributor has arrived: ready for the next call
               last_flag = last;
             }
-            if (!epi_sync(&sync_bar, sync_phase, &abort_flag, p.status)) return false;
+            if (!conv_sync(&sync_bar, sync_phase, &abort_flag, p.status)) return false;
             if (last_flag) {
               __threadfence();
               if (n < p.N) {
@@ -415,75 +520,56 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
 
     bool ok = true;
     for (Walk it(b0, b1, p.KB); ok && !it.done(); it.next()) {
-      const int s = it.q % NR;
+      const int s = it.q % NW;
       const int a = it.q % NA;
-      if (!mbar_wait_all(&full_bar[s], (uint32_t)((it.q / NR) & 1), &abort_flag, p.status)) {
+      if (!mbar_wait_all(&wfull_bar[s], (uint32_t)((it.q / NW) & 1), &abort_flag, p.status)) {
         ok = false;
         break;
       }
       if (it.q >= NA) {
-        // The operand slot is free once the MMAs of stage q - NA have completed; that stage retires now.
-        if (!mbar_wait_all(&mma_bar[a], (uint32_t)(((it.q - NA) / NA) & 1), &abort_flag, p.status) || !retire()) {
+        // The A stage is free once the MMAs of stage q - NA have completed; that stage retires now.
+        const int qo = it.q - NA;
+        if (!mbar_wait_lane0(&adone_bar[a], (uint32_t)((qo / NA) & 1), &abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (!retire()) {
           ok = false;
           break;
         }
       }
       const bool have = 2 * it.t + half < p.tiles64;   // this packed tile exists (warp-uniform)
-      const uint8_t* wsrc = raw + s * L::kRaw + L::kXBox + half * kHalfBytes;
+      if (have && unit < it.ns) {
+        const uint8_t* wsrc = wring + s * kWStage + half * kHalfBytes + unit * kPackSlab;
 #pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        const int unit = 2 * upair + jj;
-        if (!(have && unit < it.ns)) continue;
-        const uint4 u = lds128(wsrc + unit * kPackSlab + offA);
-        const uint4 v = lds128(wsrc + unit * kPackSlab + offB);
-        // own row's words of chunks cA and cB, and the partner row's
-        const uint32_t oa_lo = jr ? u.y : u.x, oa_hi = jr ? u.w : u.z;
-        const uint32_t ob_lo = jr ? v.y : v.x, ob_hi = jr ? v.w : v.z;
-        const uint32_t pa_lo = jr ? u.x : u.y, pa_hi = jr ? u.z : u.w;
-        const uint32_t pb_lo = jr ? v.x : v.y, pb_hi = jr ? v.z : v.w;
-        // this row's words of the partner's chunks 2 (1 - j) + bsw and 2 (1 - j) + 1 - bsw
-        const uint32_t ra_lo = __shfl_xor_sync(0xffffffffu, pa_lo, 8);
-        const uint32_t ra_hi = __shfl_xor_sync(0xffffffffu, pa_hi, 8);
-        const uint32_t rb_lo = __shfl_xor_sync(0xffffffffu, pb_lo, 8);
-        const uint32_t rb_hi = __shfl_xor_sync(0xffffffffu, pb_hi, 8);
-        // chunks 2 j, 2 j + 1 (own) and 2 (1 - j), 2 (1 - j) + 1 (received), each in k order
-        const uint32_t e0l = bsw ? ob_lo : oa_lo, e0h = bsw ? ob_hi : oa_hi;
-        const uint32_t e1l = bsw ? oa_lo : ob_lo, e1h = bsw ? oa_hi : ob_hi;
-        const uint32_t f0l = bsw ? rb_lo : ra_lo, f0h = bsw ? rb_hi : ra_hi;
-        const uint32_t f1l = bsw ? ra_lo : rb_lo, f1h = bsw ? ra_hi : rb_hi;
-        const uint32_t w[8] = {jr ? f0l : e0l, jr ? f0h : e0h, jr ? f1l : e1l, jr ? f1h : e1h,
-                               jr ? e0l : f0l, jr ? e0h : f0h, jr ? e1l : f1l, jr ? e1h : f1h};
-        uint32_t h[16];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) offset_bytes_to_half2_pairs(w[i], h[2 * i], h[2 * i + 1]);
-        tmem_st16(t_lane + (uint32_t)(a * kACols + 16 * unit), h);
+        for (int r = 0; r < 2; ++r) {
+          const uint4 u = lds128(wsrc + ((s16 + r) * 32 + lane) * 16);
+          uint32_t h[8];
+          offset_bytes_to_half2_pairs(u.x, h[0], h[1]);   // row g,     k 8c .. 8c+3
+          offset_bytes_to_half2_pairs(u.y, h[2], h[3]);   // row g + 8, k 8c .. 8c+3
+          offset_bytes_to_half2_pairs(u.z, h[4], h[5]);   // row g,     k 8c+4 .. 8c+7
+          offset_bytes_to_half2_pairs(u.w, h[6], h[7]);   // row g + 8, k 8c+4 .. 8c+7
+          tmem_st_16x256_x2(t_lane + ((uint32_t)(16 * r) << 16) + (uint32_t)(a * kACols + 16 * unit), h);
+        }
       }
-      uint8_t* const bst = bring + a * L::kBStage;
-#pragma unroll 2
-      for (int rep = 0; rep < L::kXPieces; ++rep) {
-        const int idx = threadIdx.x + kConvThreads * rep;
-        const int m = idx % kN, pc = idx / kN;
-        const uint4 xr = lds128(raw + s * L::kRaw + m * 128 + ((pc ^ (m & 7)) << 4));
-        uint4 h0, h1;
-        offset_bytes_to_half2_pairs(xr.x ^ 0x80808080u, h0.x, h0.y);
-        offset_bytes_to_half2_pairs(xr.y ^ 0x80808080u, h0.z, h0.w);
-        offset_bytes_to_half2_pairs(xr.z ^ 0x80808080u, h1.x, h1.y);
-        offset_bytes_to_half2_pairs(xr.w ^ 0x80808080u, h1.z, h1.w);
-        uint8_t* dst = bst + (m >> 3) * kBSbo + (2 * pc) * 128 + (m & 7) * 16;
-        *reinterpret_cast<uint4*>(dst) = h0;
-        *reinterpret_cast<uint4*>(dst + 128) = h1;
-      }
-      // Every raw value of the stage has been read and used.
+      // Every weight value of the stage has been read and used: the slot goes back to the producer.
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[s]);
+      if (lane == 0) mbar_arrive(&wempty_bar[s]);
+      // The MMAs of this stage also need its activations: see them land before handing the stage over.
+      if (!mbar_wait_all(&bfull_bar[it.q % NB], (uint32_t)((it.q / NB) & 1), &abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
       tmem_wait_st();
-      fence_async_shared();
       tc_fence_before();
-      mbar_arrive(&conv_bar[a]);
+      mbar_arrive_warp(&conv_bar[a]);
     }
     // Retire the stages still in flight.
     while (ok && !dr.done()) {
-      if (!mbar_wait_all(&mma_bar[dr.q % NA], (uint32_t)((dr.q / NA) & 1), &abort_flag, p.status) || !retire()) break;
+      if (!mbar_wait_lane0(&adone_bar[dr.q % NA], (uint32_t)((dr.q / NA) & 1), &abort_flag, p.status)) break;
+      tc_fence_after();
+      if (!retire()) break;
     }
   }
 
@@ -496,7 +582,7 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
 }
 
 template <int NT16>
-static cudaError_t launch_tc(const TcParams& p, int blocks, bool pdl, cudaStream_t stream) {
+static cudaError_t launch_tc(const TcParams& p, int blocks, cudaStream_t stream) {
   auto kern = w8a8_gemm_tc_kernel<NT16>;
   const int smem = TcLayout<NT16>::kBytes;
   cudaError_t e = ensure_smem_attribute((const void*)kern, smem);
@@ -506,12 +592,30 @@ static cudaError_t launch_tc(const TcParams& p, int blocks, bool pdl, cudaStream
   cfg.blockDim = dim3(TcLayout<NT16>::kThreads);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
+  // Always a programmatic dependent of the x16 launch just before it.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+static cudaError_t launch_x16(const int8_t* x, void* x16, long long units, bool pdl, cudaStream_t stream) {
+  long long grid = (units + 255) / 256;
+  if (grid > 8 * 152) grid = 8 * 152;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(grid < 1 ? 1 : grid));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  e = cudaLaunchKernelEx(&cfg, kern, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, x16_kernel, reinterpret_cast<const uint4*>(x), static_cast<uint4*>(x16), units);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -529,8 +633,21 @@ int tc_plan(int M, int K, int N, int blocks, int sm_count, TcPlan* plan) {
   pl.kb = K / tc::kKBlock;
   pl.units = (long long)pl.n_tiles * pl.kb;
   if (blocks == 0) {
-    // One CTA per SM: each holds all of its SM's tensor memory and most of its shared memory.
-    const long long g = sm_count > 0 ? sm_count : 152;
+    // At most one CTA per SM: each holds all of its SM's tensor memory and most of its shared
+    // memory.  With at least as many tiles as SMs, a CTA count that divides the tile count gives
+    // every CTA whole tiles, so no tile needs a combine; at M = 128 a tile's partial sums are as
+    // large as 512 k of its weight, and such a plan was measured faster (gate_up-sized, 192
+    // tiles: 96 CTAs 68 us, 152 CTAs 102 us).  Otherwise one CTA per SM.
+    const int sms = sm_count > 0 ? sm_count : 152;
+    long long g = sms;
+    if (pl.n_tiles >= sms) {
+      for (int c = sms; 2 * c >= sms; --c) {
+        if (pl.n_tiles % c == 0) {
+          g = c;
+          break;
+        }
+      }
+    }
     pl.blocks = (int)(g < pl.units ? g : pl.units);
   } else {
     if (blocks > pl.units) return W8A8_ERR_INVALID_ARG;
@@ -538,33 +655,41 @@ int tc_plan(int M, int K, int N, int blocks, int sm_count, TcPlan* plan) {
   }
   if (pl.mma_n == 64) {
     pl.threads = tc::TcLayout<4>::kThreads;
-    pl.stages = tc::TcLayout<4>::kRawStages;
+    pl.stages = tc::TcLayout<4>::kWStages;
     pl.smem_bytes = tc::TcLayout<4>::kBytes;
   } else {
     pl.threads = tc::TcLayout<8>::kThreads;
-    pl.stages = tc::TcLayout<8>::kRawStages;
+    pl.stages = tc::TcLayout<8>::kWStages;
     pl.smem_bytes = tc::TcLayout<8>::kBytes;
   }
   pl.stage_units = tc::kStageUnits;
+  // Workspace: header, counters, int32 planes, then the fp16 activations.  The counters and planes
+  // are zero between calls and the activations are not, so every region sits at an offset that
+  // does not depend on M: the planes are sized for MMA N = 128 whatever this call's M, and the
+  // activations come last.  No call of either arm then finds its zeroed region written by another
+  // (the decode arm's words, at most 32 KiB per 128 rows of N, end before the planes do).
   pl.counters_offset = kWsHeaderBytes;
   pl.partials_offset = pl.counters_offset + ((size_t)pl.n_tiles * sizeof(uint32_t) + 255) / 256 * 256;
-  pl.workspace_bytes = pl.partials_offset + (size_t)pl.n_tiles * pl.mma_n * tc::kTileRows * sizeof(int);
+  pl.x16_offset = pl.partials_offset + (size_t)pl.n_tiles * kTcMaxM * tc::kTileRows * sizeof(int);
+  pl.workspace_bytes = pl.x16_offset + ((size_t)M * K * 2 + 255) / 256 * 256;
   *plan = pl;
   return W8A8_OK;
 }
 
 cudaError_t tc_launch(const TcPlan& pl, const int8_t* x, const float* xs, const void* wp, const float* wsc, void* out,
                       int M, int K, int N, void* ws, bool pdl, cudaStream_t stream) {
-  tc::TcParams p;
-  // Activation tensor map: [M rows, K bytes], box of 128 bytes x mma_n rows (rows >= M read as 0).
-  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-  const cuuint64_t strides[1] = {(cuuint64_t)K};
-  const cuuint32_t box[2] = {128u, (cuuint32_t)pl.mma_n};
-  const cuuint32_t estr[2] = {1u, 1u};
-  cudaError_t e = encode_tensor_map_2d(&p.xmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<int8_t*>(x), dims, strides,
-                                       box, estr, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (e != cudaSuccess) return e;
   uint8_t* const w = static_cast<uint8_t*>(ws);
+  void* const x16 = w + pl.x16_offset;
+  tc::TcParams p;
+  // fp16 activations in the workspace (k permuted inside each 32-k unit, as the weight in tensor
+  // memory): [M rows, K], box of 64 x mma_n (rows >= M read as 0).
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)tc::kBoxK, (cuuint32_t)pl.mma_n};
+  const cuuint32_t estr[2] = {1u, 1u};
+  cudaError_t e = encode_tensor_map_2d(&p.xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, dims, strides, box, estr,
+                                       CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
   p.wp = static_cast<const uint8_t*>(wp);
   p.x_scale = xs;
   p.w_scale = wsc;
@@ -577,8 +702,9 @@ cudaError_t tc_launch(const TcPlan& pl, const int8_t* x, const float* xs, const 
   p.N = N;
   p.KB = pl.kb;
   p.tiles64 = pl.tiles64;
-  p.pdl = pdl ? 1 : 0;
-  return pl.mma_n == 64 ? tc::launch_tc<4>(p, pl.blocks, pdl, stream) : tc::launch_tc<8>(p, pl.blocks, pdl, stream);
+  e = tc::launch_x16(x, x16, (long long)M * K / 32, pdl, stream);
+  if (e != cudaSuccess) return e;
+  return pl.mma_n == 64 ? tc::launch_tc<4>(p, pl.blocks, stream) : tc::launch_tc<8>(p, pl.blocks, stream);
 }
 
 }  // namespace w8a8

@@ -131,13 +131,17 @@ def test_tensor_memory_arm_plan():
     p = lib8.w8a8_plan(128, 4096, 1536)
     assert p["tensor_memory"] == 1 and p["tile_rows"] == 128 and p["n8_tiles"] == 16
     assert p["n_tiles"] == 12 and p["k_blocks"] == 128 and p["slabs"] == 12 * 128
-    assert p["blocks"] == 152 and p["threads"] == 320 and p["smem_bytes"] <= 227 * 1024
+    assert p["blocks"] == 152 and p["threads"] == 608 and p["smem_bytes"] <= 227 * 1024
     q = lib8.w8a8_plan(33, 4096, 320)
-    assert q["n8_tiles"] == 8 and q["n_tiles"] == 3 and q["threads"] == 352
+    assert q["n8_tiles"] == 8 and q["n_tiles"] == 3 and q["threads"] == 640
     assert lib8.w8a8_plan(32, 4096, 320)["tensor_memory"] == 0
-    # header, counters (one per tile, padded to 256 bytes), int32 planes [tile][mma_n][128]
-    assert p["workspace_bytes"] == 256 + 256 + 12 * 128 * 128 * 4
-    assert q["workspace_bytes"] == 256 + 256 + 3 * 64 * 128 * 4
+    # header, counters (one per tile, padded to 256 bytes), int32 planes [tile][128][128] whatever
+    # M (so that no region moves with M), then the fp16 activations [M][K]
+    assert p["workspace_bytes"] == 256 + 256 + 12 * 128 * 128 * 4 + 128 * 4096 * 2
+    assert q["workspace_bytes"] == 256 + 256 + 3 * 128 * 128 * 4 + 33 * 4096 * 2
+    # with at least as many 128-row tiles as SMs, a CTA count dividing the tile count (whole tiles)
+    assert lib8.w8a8_plan(128, 4096, 24576)["blocks"] == 96
+    assert lib8.w8a8_plan(128, 12288, 4096)["blocks"] == 152
     # the size query for M_max covers both arms
     big = lib8.w8a8_workspace_bytes(128, 4096, 1536)
     assert all(lib8.w8a8_plan(M, 4096, 1536)["workspace_bytes"] <= big for M in range(1, 129))
@@ -156,45 +160,51 @@ def test_tensor_memory_arm_split_bounds(M, K, N, blocks):
         assert all(b0 // KB == (b1 - 1) // KB for b0, b1 in zip(b[:-1], b[1:]))
 
 
-def test_tensor_memory_arm_row_assembly_emulated():
-    # CPU replay of the converter's index arithmetic: for every tensor-memory lane (tile row) the
-    # two 16-byte chunk reads, the exchange with lane ^ 8 and the selects must yield that row's 32
-    # weights of a 32-k unit in k order, from the packed layout the oracle writes.
-    K, N = 64, 128
+def test_tensor_memory_arm_operands_emulated():
+    # CPU replay of the tensor-memory arm's operand layout: each converter thread writes its packed
+    # 16-byte chunk with the 16x256b store (thread t: lanes t/4 and t/4 + 8, columns 2(t%4), 2(t%4)+1
+    # and those plus 8), and the fp16 activation copy reorders each 32-k unit's groups of four as
+    # 0, 2, 4, 6, 1, 3, 5, 7.  Column j of a row then pairs with activation positions 2j, 2j + 1, and
+    # the dot product over all columns must equal x @ W exactly.
+    M, K, N = 3, 64, 128
+    x = synth.uniform_int8(6, "tc.x", (M, K), lo=-128, hi=127).astype(np.int64)
     W = synth.uniform_int8(5, "tc.W", (K, N), lo=-128, hi=127)
     packed = oracle.w8a8_pack(W).astype(np.int64)
     KB = K // 32
 
-    def words(off):
-        return [int(packed[off + 4 * i]) | int(packed[off + 4 * i + 1]) << 8 |
-                int(packed[off + 4 * i + 2]) << 16 | int(packed[off + 4 * i + 3]) << 24 for i in range(4)]
+    def sbyte(b):
+        b ^= 0x80
+        return b - 256 if b >= 128 else b
 
+    # tensor memory A: [row][unit][column j] -> (k0, k1) weight values
+    A = np.zeros((128, KB, 16, 2), np.int64)
     for quad in range(4):
         half = quad >> 1
         for unit in range(KB):
-            st = []
-            for lane in range(32):
-                s16, g = 2 * (quad & 1) + (lane >> 4), lane & 7
-                jr, bsw = (lane >> 3) & 1, (g >> 1) & 1
-                base = (half * KB + unit) * 2048
-                u = words(base + (s16 * 32 + 4 * g + 2 * jr + bsw) * 16)
-                v = words(base + (s16 * 32 + 4 * g + 2 * jr + 1 - bsw) * 16)
-                own = [(u[1], u[3]) if jr else (u[0], u[2]), (v[1], v[3]) if jr else (v[0], v[2])]
-                other = [(u[0], u[2]) if jr else (u[1], u[3]), (v[0], v[2]) if jr else (v[1], v[3])]
-                st.append((jr, bsw, own, other))
-            for lane in range(32):
-                jr, bsw, own, _ = st[lane]
-                ra, rb = st[lane ^ 8][3]
-                e = [own[1], own[0]] if bsw else own
-                f = [rb, ra] if bsw else [ra, rb]
-                chunks = f + e if jr else e + f
-                vals = []
-                for lo, hi in chunks:
-                    for w in (lo, hi):
-                        vals += [(((w >> (8 * i)) & 0xFF) ^ 0x80) - 256 * ((((w >> (8 * i)) & 0xFF) ^ 0x80) >= 128)
-                                 for i in range(4)]
-                row = 32 * quad + lane
-                assert vals == W[32 * unit:32 * unit + 32, row].tolist()
+            for r in range(2):
+                s16 = 2 * (quad & 1) + r
+                for t in range(32):
+                    off = (half * KB + unit) * 2048 + (s16 * 32 + t) * 16
+                    words = [[sbyte(int(packed[off + 4 * wi + b])) for b in range(4)] for wi in range(4)]
+                    # four conversions -> eight registers of two values (natural pairs)
+                    h = []
+                    for wi in range(4):
+                        h += [words[wi][0:2], words[wi][2:4]]
+                    g, c = t // 4, t % 4
+                    lane_of = [g, g, g + 8, g + 8, g, g, g + 8, g + 8]
+                    col_of = [2 * c, 2 * c + 1, 2 * c, 2 * c + 1, 8 + 2 * c, 9 + 2 * c, 8 + 2 * c, 9 + 2 * c]
+                    # registers: v0 = h0 (row g), v1 = h1, v2 = h2 (row g+8), v3 = h3, v4 = h4, ...
+                    for v in range(8):
+                        A[32 * quad + 16 * r + lane_of[v], unit, col_of[v]] = h[v]
+    # fp16 activation copy: groups of four reordered 0, 2, 4, 6, 1, 3, 5, 7 within each unit
+    order = [0, 2, 4, 6, 1, 3, 5, 7]
+    B = np.zeros((M, KB, 32), np.int64)
+    for m in range(M):
+        for unit in range(KB):
+            for gi, src in enumerate(order):
+                B[m, unit, 4 * gi:4 * gi + 4] = x[m, 32 * unit + 4 * src:32 * unit + 4 * src + 4]
+    got = np.einsum("nujq,mujq->mn", A, B.reshape(M, KB, 16, 2))
+    np.testing.assert_array_equal(got, x @ W.astype(np.int64))
 
 
 def test_two_element_combine_words():
