@@ -402,6 +402,37 @@ def time_quantisation_rows(peak):
     return rows
 
 
+def time_tensor_memory_arm(args, dev, hbm_peak):
+    """The 32 < M <= 128 arm (tcgen05) at M = 128 on the fused-QKV-like shape and the gate_up MLP
+    shape: the same rotating-weight graph replays as the headline, reported beside it.  At M = 128
+    a weight byte feeds 256 flops, so the line gives both the HBM fraction (weight bytes) and the
+    tensor fraction (2 M N K flops against the measured bf16 peak; the fp16 kind has the same
+    nominal rate)."""
+    import torch
+
+    peaks = {}
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            peaks = json.load(f)
+    tensor_peak = float(peaks.get("bf16_tflops", 1900.0))
+    rows = []
+    for (M, K, N, dist, seed) in ((128, 4096, 1536, "uniform", 5128), (128, 4096, 24576, "mlp", 5)):
+        r = time_gemm(M, K, N, dist, seed, min(args.steps, 100), args.warmup, device=dev, want_e2e=False)
+        r.pop("inputs")
+        us = r["us_median"]
+        gbs = r["wbytes"] / (us * 1e-6) / 1e9
+        tflops = 2.0 * M * N * K / (us * 1e-6) / 1e12
+        rows.append({"M": M, "K": K, "N": N, "kernel": r["kernel"], "blocks": r["blocks"],
+                     "us_per_call": {"median": round(us, 3), "p90": round(r["us_p90"], 3)},
+                     "weight_GBps": round(gbs, 1), "frac_of_measured_hbm": round(gbs / hbm_peak, 4),
+                     "tflops": round(tflops, 1), "frac_of_measured_bf16": round(tflops / tensor_peak, 4),
+                     "launches_per_call": 2})
+        del r
+        torch.cuda.empty_cache()
+    return rows
+
+
 def time_q8(T, K, N, iters=200, seed=7, flags=0):
     """Median us per Q8_0 read in a graph of calls over rotating weight sets (not L2-resident)."""
     import torch
@@ -519,6 +550,7 @@ def run_ours(args):
         if not args.no_q8:
             out["q8_0"] = [time_q8(T, K8, N8, flags=f) for (K8, N8) in ((4096, 320), (320, 4096)) for T in (1, 4, 6)
                            for f in (0, lib8.W8A8_FLAG_PDL)]
+        out["tensor_memory_arm"] = time_tensor_memory_arm(args, dev, peak)
         out["read_ceiling"] = time_read_ceiling(dev)
         if not args.no_q8:
             out["quantisation"] = time_quantisation_rows(peak)
