@@ -47,6 +47,10 @@ def lib():
         L.oracle_q8_0_gemv.restype = None
         L.oracle_q8_0_norms.argtypes = [c_p, c_p, c_p, c_i, c_i, c_i, c_p, c_p]
         L.oracle_q8_0_norms.restype = None
+        L.oracle_q8_0_rms_gemv.argtypes = [c_p, c_p, ctypes.c_double, c_p, c_p, c_i, c_i, c_i, c_p, c_p]
+        L.oracle_q8_0_rms_gemv.restype = None
+        L.oracle_q8_0_rms_xg_norms.argtypes = [c_p, c_p, c_i, c_i, c_p]
+        L.oracle_q8_0_rms_xg_norms.restype = None
         L.oracle_q8_0_split_from_blocks.argtypes = [c_p, c_i, c_i, c_p, c_p]
         L.oracle_q8_0_split_from_blocks.restype = None
         L.oracle_w8a8_packed_bytes.argtypes = [c_i, c_i]
@@ -196,6 +200,35 @@ def q8_0_bound(x_bits, q, d_bits, rel: float = 2e-3) -> np.ndarray:
     """Per-output error bound [T,N]: rel * ||x_t||_2 * ||w_n||_2."""
     xn, wn = q8_0_norms(x_bits, q, d_bits)
     return rel * np.outer(xn, wn)
+
+
+def q8_0_rms_gemv(x_bits: np.ndarray, g_bits: np.ndarray, eps: float, q: np.ndarray, d_bits: np.ndarray):
+    """(y float64 [T,N], rs float64 [T]): y[t,n] = rs[t] * sum_k (x[t,k] g[k]) (d[n,k/32] q[n,k]),
+    rs[t] = 1 / sqrt(sum_k x[t,k]^2 / K + eps) (oracle.c: oracle_q8_0_rms_gemv)."""
+    x_bits = _c(x_bits, np.uint16)
+    g_bits = _c(g_bits, np.uint16)
+    q = _c(q, np.int8)
+    d_bits = _c(d_bits, np.uint16)
+    T, K = x_bits.shape
+    N = q.shape[0]
+    assert g_bits.shape == (K,)
+    y = np.zeros((T, N), dtype=np.float64)
+    rs = np.zeros(T, dtype=np.float64)
+    lib().oracle_q8_0_rms_gemv(_ptr(x_bits), _ptr(g_bits), float(eps), _ptr(q), _ptr(d_bits), T, K, N, _ptr(y),
+                               _ptr(rs))
+    return y, rs
+
+
+def q8_0_rms_bound(x_bits, g_bits, eps, q, d_bits, rel: float = 4e-3) -> np.ndarray:
+    """Per-output error bound of the RMS-norm read: rel * rs[t] * ||x_t * g||_2 * ||w_n||_2."""
+    x_bits = _c(x_bits, np.uint16)
+    g_bits = _c(g_bits, np.uint16)
+    T, K = x_bits.shape
+    xg = np.zeros(T, dtype=np.float64)
+    lib().oracle_q8_0_rms_xg_norms(_ptr(x_bits), _ptr(g_bits), T, K, _ptr(xg))
+    _, wn = q8_0_norms(x_bits, q, d_bits)
+    _, rs = q8_0_rms_gemv(x_bits, g_bits, eps, q[:1], d_bits[:1])
+    return rel * (rs * xg)[:, None] * wn[None, :]
 
 
 def q8_0_split_from_blocks(blocks: np.ndarray, K: int, N: int):

@@ -191,6 +191,49 @@ void oracle_q8_0_norms(const uint16_t* x, const int8_t* q, const uint16_t* d,
     }
 }
 
+/* Q8_0 read with an RMS-norm prologue.  [Q8_0] section "What changed": the down kernel stages
+ * R' * w_norm unscaled together with the sums of squares of the rows, and the last work-group to
+ * arrive applies rs per stream.  Generic reading (the design notes list it): rs[t] is the inverse
+ * root mean square of x's row t, 1 / sqrt(sum_k x[t][k]^2 / K + eps), and
+ *   y[t][n] = rs[t] * sum_k (x[t][k] * g[k]) * (d[n][k/32] * q[n][k]),
+ * all in double from the very bf16 / fp16 / int8 bytes the kernel reads.  x: bf16 bits [T,K];
+ * g: bf16 bits [K] (w_norm); q, d as in oracle_q8_0_gemv; rs: out [T], may be NULL. */
+void oracle_q8_0_rms_gemv(const uint16_t* x, const uint16_t* g, double eps, const int8_t* q,
+                          const uint16_t* d, int T, int K, int N, double* y, double* rs) {
+    int nb = K / 32;
+    for (int t = 0; t < T; ++t) {
+        double ss = 0.0;
+        for (int k = 0; k < K; ++k) {
+            double v = oracle_bf16_to_f64(x[(size_t)t * K + k]);
+            ss += v * v;
+        }
+        double r = 1.0 / sqrt(ss / (double)K + eps);
+        if (rs) rs[t] = r;
+        for (int n = 0; n < N; ++n) {
+            double s = 0.0;
+            for (int k = 0; k < K; ++k) {
+                double xg = oracle_bf16_to_f64(x[(size_t)t * K + k]) * oracle_bf16_to_f64(g[k]);
+                double w = oracle_f16_to_f64(d[(size_t)n * nb + k / 32]) * (double)q[(size_t)n * K + k];
+                s += xg * w;
+            }
+            y[(size_t)t * N + n] = r * s;
+        }
+    }
+}
+
+/* xgnorm[t] = ||x_t * g||_2 (elementwise product), for the per-output error bound of the
+ * RMS-norm read. */
+void oracle_q8_0_rms_xg_norms(const uint16_t* x, const uint16_t* g, int T, int K, double* xgnorm) {
+    for (int t = 0; t < T; ++t) {
+        double s = 0.0;
+        for (int k = 0; k < K; ++k) {
+            double v = oracle_bf16_to_f64(x[(size_t)t * K + k]) * oracle_bf16_to_f64(g[k]);
+            s += v * v;
+        }
+        xgnorm[t] = sqrt(s);
+    }
+}
+
 /* ggml-style interleaved Q8_0 rows (per block: fp16 scale, then 32 int8 quants; 34 bytes)
  * -> the split layout (all quants [N][K], then all scales [N][K/32]).  [Q8_0] "What changed":
  * "the same bytes as ggml's 34-byte blocks, reordered". */

@@ -430,3 +430,88 @@ def test_q8_0_blocks_and_split_layout_are_inverse():
     q2, d2 = oracle.q8_0_split_from_blocks(blocks, K, N)
     np.testing.assert_array_equal(q2, q)
     np.testing.assert_array_equal(d2, d)
+
+
+# --------------------------------------------------------------------------------------------
+# Q8_0 read with an RMS-norm prologue (rs * (x * g) @ w, rs the inverse RMS of x's row)
+# --------------------------------------------------------------------------------------------
+
+def _xg_inputs(T, K, N, seed):
+    x, q, d = synth.q8_0_inputs(T, K, N, seed=seed)
+    g = torch.tensor(synth.uniform_f32(seed, "pin.g", (K,), 0.5, 1.5)).to(torch.bfloat16)
+    return (x.view(torch.int16).numpy().view(np.uint16), g.view(torch.int16).numpy().view(np.uint16), q,
+            d.view(np.uint16), x, g, d)
+
+
+def test_q8_0_rms_brute_force_with_python_floats():
+    # Independent restatement: Python floats from torch's bf16 decoding, math.fsum for the sums.
+    import math
+    T, K, N = 2, 64, 3
+    xb, gb, q, db, x, g, d = _xg_inputs(T, K, N, seed=3)
+    eps = 1e-5
+    y, rs = oracle.q8_0_rms_gemv(xb, gb, eps, q, db)
+    xf, gf = x.double().numpy(), g.double().numpy()
+    for t in range(T):
+        r = 1.0 / math.sqrt(math.fsum(float(v) * float(v) for v in xf[t]) / K + eps)
+        assert abs(r - rs[t]) <= 1e-14 * r
+        for n in range(N):
+            s = math.fsum(float(xf[t, k]) * float(gf[k]) * float(d[n, k // 32]) * int(q[n, k]) for k in range(K))
+            assert abs(r * s - y[t, n]) <= 1e-12 * max(1.0, abs(r * s))
+
+
+def test_q8_0_rms_gamma_one_reduces_to_the_plain_read():
+    T, K, N = 3, 320, 7
+    xb, _, q, db, *_ = _xg_inputs(T, K, N, seed=4)
+    ones = _bf16_bits(np.ones(K))
+    y, rs = oracle.q8_0_rms_gemv(xb, ones, 1e-6, q, db)
+    np.testing.assert_array_equal(y, rs[:, None] * oracle.q8_0_gemv(xb, q, db))
+
+
+def test_q8_0_rms_is_scale_invariant_without_eps():
+    # RMS normalisation: doubling x (exact in bf16 and fp64) leaves every output bit unchanged when
+    # eps = 0; a missing rs, rs from x * g, or a wrong power would not.
+    T, K, N = 2, 128, 5
+    xb, gb, q, db, x, g, d = _xg_inputs(T, K, N, seed=5)
+    x2 = (x.float() * 2).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    y1, rs1 = oracle.q8_0_rms_gemv(xb, gb, 0.0, q, db)
+    y2, rs2 = oracle.q8_0_rms_gemv(x2, gb, 0.0, q, db)
+    np.testing.assert_array_equal(y1, y2)
+    np.testing.assert_array_equal(rs2, rs1 / 2)
+
+
+def test_q8_0_rms_closed_forms():
+    # Constant rows: x = c, g = 1, q = 1: rs = 1 / sqrt(c^2 + eps), y = rs * c * 32 * sum_b d[n, b].
+    T, K, N = 2, 96, 4
+    d = synth.uniform_f16(9, "pin.d", (N, K // 32), 1e-3, 1e-2)
+    q = np.ones((N, K), np.int8)
+    eps = 0.25
+    for c in (0.5, -3.0):
+        xb = _bf16_bits(np.full((T, K), c))
+        y, rs = oracle.q8_0_rms_gemv(xb, _bf16_bits(np.ones(K)), eps, q, d.view(np.uint16))
+        r = 1.0 / np.sqrt(c * c + eps)
+        np.testing.assert_allclose(rs, r, rtol=1e-15)
+        np.testing.assert_allclose(y, np.broadcast_to(r * c * 32.0 * d.astype(np.float64).sum(axis=1), (T, N)),
+                                   rtol=1e-14)
+    # One-hot x at k0 with weight g[k0]: rs = 1 / sqrt(x^2 / K + eps), y = rs * x * g[k0] * d q.
+    K, N = 64, 3
+    q = synth.uniform_int8(10, "pin.q", (N, K))
+    d = synth.uniform_f16(10, "pin.d", (N, K // 32), 1e-3, 1e-2)
+    g = np.array([0.5 + k / 64 for k in range(K)])
+    for k0 in (0, 33, 63):
+        xv = np.zeros((1, K))
+        xv[0, k0] = 4.0
+        y, rs = oracle.q8_0_rms_gemv(_bf16_bits(xv), _bf16_bits(g), 1e-3, q, d.view(np.uint16))
+        r = 1.0 / np.sqrt(16.0 / K + 1e-3)
+        np.testing.assert_allclose(rs[0], r, rtol=1e-15)
+        np.testing.assert_allclose(y[0], r * 4.0 * g[k0] * d[:, k0 // 32].astype(np.float64) * q[:, k0], rtol=1e-14)
+
+
+def test_q8_0_rms_bound_scales_with_rs_and_the_norms():
+    T, K, N = 2, 64, 3
+    xb, gb, q, db, x, g, d = _xg_inputs(T, K, N, seed=11)
+    b = oracle.q8_0_rms_bound(xb, gb, 1e-6, q, db)
+    _, rs = oracle.q8_0_rms_gemv(xb, gb, 1e-6, q, db)
+    xg = (x.double() * g.double()).numpy()
+    w = d.astype(np.float64).repeat(32, axis=1) * q.astype(np.float64)
+    expect = 4e-3 * rs[:, None] * np.sqrt((xg * xg).sum(axis=1))[:, None] * np.sqrt((w * w).sum(axis=1))[None, :]
+    np.testing.assert_allclose(b, expect, rtol=1e-13)
