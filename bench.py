@@ -433,14 +433,23 @@ def time_tensor_memory_arm(args, dev, hbm_peak):
     return rows
 
 
-def time_q8(T, K, N, iters=200, seed=7, flags=0):
-    """Median us per Q8_0 read in a graph of calls over rotating weight sets (not L2-resident)."""
+def time_q8(T, K, N, iters=200, seed=7, flags=0, rms=False):
+    """Median us per Q8_0 read in a graph of calls over rotating weight sets (not L2-resident);
+    rms=True times the RMS-norm variant (q8_0_gemv_rms) on the same weights."""
     import torch
 
     import int8_weight_gemm_gb300 as lib8
     import synth
 
     x, q, d = synth.q8_0_inputs(T, K, N, seed=seed)
+    gd = torch.ones(K, dtype=torch.bfloat16, device="cuda") * 0.75
+
+    def read(xd, qi, di, ws, y, stream):
+        if rms:
+            lib8.q8_0_gemv_rms(xd, gd, 1e-6, qi, di, ws, y=y, flags=flags, stream=stream)
+        else:
+            lib8.q8_0_gemv(xd, qi, di, ws, y=y, flags=flags, stream=stream)
+
     props = torch.cuda.get_device_properties(0)
     l2 = getattr(props, "L2_cache_size", 128 << 20)
     nbytes = N * K + 2 * N * (K // 32)
@@ -455,12 +464,12 @@ def time_q8(T, K, N, iters=200, seed=7, flags=0):
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         for i in range(R):
-            lib8.q8_0_gemv(xd, qs[i], ds[i], ws, y=y, flags=flags, stream=s)
+            read(xd, qs[i], ds[i], ws, y, s)
     s.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         for i in range(R):
-            lib8.q8_0_gemv(xd, qs[i], ds[i], ws, y=y, flags=flags, stream=s)
+            read(xd, qs[i], ds[i], ws, y, s)
     for _ in range(5):
         g.replay()
     torch.cuda.synchronize()
@@ -475,7 +484,7 @@ def time_q8(T, K, N, iters=200, seed=7, flags=0):
         s.synchronize()
         samples.append(a.elapsed_time(b) * 1e3 / R)
     samples.sort()
-    return {"T": T, "K": K, "N": N, "flags": flags, "us_median": statistics.median(samples),
+    return {"T": T, "K": K, "N": N, "flags": flags, "rms_norm": rms, "us_median": statistics.median(samples),
             "us_p90": samples[int(0.9 * (len(samples) - 1))], "weight_bytes": nbytes,
             "GBps": nbytes / statistics.median(samples) / 1e3}
 
@@ -550,6 +559,9 @@ def run_ours(args):
         if not args.no_q8:
             out["q8_0"] = [time_q8(T, K8, N8, flags=f) for (K8, N8) in ((4096, 320), (320, 4096)) for T in (1, 4, 6)
                            for f in (0, lib8.W8A8_FLAG_PDL)]
+            # the RMS-norm variant (q8_0_gemv_rms) on the same reads
+            out["q8_0"] += [time_q8(6, K8, N8, flags=f, rms=True) for (K8, N8) in ((4096, 320), (320, 4096))
+                            for f in (0, lib8.W8A8_FLAG_PDL)]
         out["tensor_memory_arm"] = time_tensor_memory_arm(args, dev, peak)
         out["read_ceiling"] = time_read_ceiling(dev)
         if not args.no_q8:
@@ -654,6 +666,7 @@ def run_sweep(args):
         for T in (1, 4, 6):
             for flags in flags_list:
                 print(json.dumps(time_q8(T, K8, N8, flags=flags)), flush=True)
+                print(json.dumps(time_q8(T, K8, N8, flags=flags, rms=True)), flush=True)
 
 
 def run_ncu_driver(args):

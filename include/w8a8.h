@@ -266,6 +266,22 @@ size_t q8_0_workspace_bytes(int T_max, int K, int N);
 int q8_0_gemv(const void* x, const int8_t* q, const void* d, void* y, int T, int K, int N,
               unsigned flags, void* ws, size_t ws_bytes, void* stream);
 
+/* The Q8_0 read with an RMS-norm prologue:
+ *   y[t][n] = bf16_rne( rs[t] * sum_k bf16(x[t][k] * gamma[k]) * (d[n][k/32] * q[n][k]) ),
+ *   rs[t]   = 1 / sqrt(sum_k x[t][k]^2 / K + eps),
+ * the generic form of "sycl: STRATA_HC_Q8=1 reads the Q8_0 hyper-connection projections", section
+ * "What changed" (the down kernel stages R' * w_norm unscaled with the rows' sums of squares, and
+ * the last work-group to arrive applies rs per stream).  The product x * gamma is exact in fp32 and
+ * rounded once to bf16 (the MMA's operand); the sums of squares are fp32 in a fixed order; rs is
+ * IEEE division and square root.  Replays are bit-identical.
+ *  gamma  [K] bf16 (the norm weight), 16-byte aligned; read before the dependency wait under
+ *         W8A8_FLAG_PDL, like q and d (a weight).
+ *  eps    finite and >= 0, else INVALID_ARG.
+ *  Everything else, the workspace (q8_0_workspace_bytes) and the errors as q8_0_gemv. */
+int q8_0_gemv_rms(const void* x, const void* gamma, float eps, const int8_t* q, const void* d,
+                  void* y, int T, int K, int N, unsigned flags, void* ws, size_t ws_bytes,
+                  void* stream);
+
 #ifdef __cplusplus
 }
 #endif

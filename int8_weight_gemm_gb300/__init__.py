@@ -24,6 +24,7 @@ __all__ = [
     "w8a8_pack_weights",
     "w8a8_gemm",
     "q8_0_gemv",
+    "q8_0_gemv_rms",
     "w8a8_plan",
     "w8a8_split_bounds",
     "w8a8_read_probe",
@@ -84,6 +85,8 @@ SIGNATURES = {
     "q8_0_split_from_blocks": ([_c_p, _c_p, _c_p, _c_i, _c_i, _c_p], _c_i),
     "q8_0_blocks_from_split": ([_c_p, _c_p, _c_p, _c_i, _c_i, _c_p], _c_i),
     "q8_0_gemv": ([_c_p, _c_p, _c_p, _c_p, _c_i, _c_i, _c_i, ctypes.c_uint, _c_p, _c_sz, _c_p], _c_i),
+    "q8_0_gemv_rms": ([_c_p, _c_p, ctypes.c_float, _c_p, _c_p, _c_p, _c_i, _c_i, _c_i, ctypes.c_uint, _c_p, _c_sz, _c_p],
+                      _c_i),
 }
 
 _lib = None
@@ -233,6 +236,20 @@ def q8_0_gemv(x, q, d, ws, y=None, flags: int = 0, stream=None):
     rc = lib().q8_0_gemv(_ptr(x), _ptr(q), _ptr(d), _ptr(y), T, K, N, flags, _ptr(ws), _nbytes(ws),
                          _stream(stream))
     _check("q8_0_gemv", rc)
+    return y
+
+
+def q8_0_gemv_rms(x, gamma, eps: float, q, d, ws, y=None, flags: int = 0, stream=None):
+    """y[T,N] bf16 = rs * (x * gamma) [T,K] times the Q8_0 weights, rs[t] = 1 / sqrt(mean_k x[t,k]^2 + eps)."""
+    import torch
+
+    T, K = x.shape
+    N = q.shape[0]
+    if y is None:
+        y = torch.empty((T, N), dtype=torch.bfloat16, device=x.device)
+    rc = lib().q8_0_gemv_rms(_ptr(x), _ptr(gamma), float(eps), _ptr(q), _ptr(d), _ptr(y), T, K, N, flags, _ptr(ws),
+                             _nbytes(ws), _stream(stream))
+    _check("q8_0_gemv_rms", rc)
     return y
 
 

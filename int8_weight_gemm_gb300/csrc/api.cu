@@ -276,4 +276,22 @@ int q8_0_gemv(const void* x, const int8_t* q, const void* d, void* y, int T, int
   return W8A8_OK;
 }
 
+int q8_0_gemv_rms(const void* x, const void* gamma, float eps, const int8_t* q, const void* d, void* y, int T, int K,
+                  int N, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
+  if (!x || !gamma || !q || !d || !y || !ws) return W8A8_ERR_INVALID_ARG;
+  if (flags & ~(unsigned)W8A8_FLAG_PDL) return W8A8_ERR_INVALID_ARG;
+  if (!(eps >= 0.0f) || !(eps <= 3.0e38f)) return W8A8_ERR_INVALID_ARG;   // finite, not negative (NaN fails too)
+  Q8Plan pl;
+  int rc = q8_plan(T, K, N, &pl);
+  if (rc != W8A8_OK) return rc;
+  if (!aligned(x, 16) || !aligned(gamma, 16) || !aligned(q, 16) || !aligned(d, 2) || !aligned(y, 2) ||
+      !aligned(ws, 256))
+    return W8A8_ERR_MISALIGNED;
+  if (ws_bytes < pl.workspace_bytes) return W8A8_ERR_WORKSPACE_TOO_SMALL;
+  cudaError_t e = q8_launch(pl, x, q, d, y, T, K, N, ws, (flags & W8A8_FLAG_PDL) != 0, static_cast<cudaStream_t>(stream),
+                            gamma, eps);
+  if (e != cudaSuccess) return cuda_fail(e, "q8_0_gemv_rms");
+  return W8A8_OK;
+}
+
 }  // extern "C"

@@ -67,8 +67,9 @@ struct Q8Plan {
 };
 
 int q8_plan(int T, int K, int N, Q8Plan* plan);
+// gamma != NULL: the RMS-norm variant (norm weight gamma [K] bf16, epsilon eps).
 cudaError_t q8_launch(const Q8Plan& pl, const void* x, const int8_t* q, const void* d, void* y, int T, int K, int N,
-                      void* ws, bool pdl, cudaStream_t stream);
+                      void* ws, bool pdl, cudaStream_t stream, const void* gamma = nullptr, float eps = 0.f);
 
 // Encode a 2-D tiled tensor map through the driver entry point (no link-time libcuda dependency).
 cudaError_t encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType type, void* base, const cuuint64_t* dims,

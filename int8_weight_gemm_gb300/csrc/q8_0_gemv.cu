@@ -12,6 +12,13 @@
 // ascending k.  Warps of a CTA split the CTA's k range into contiguous runs and are summed in warp
 // order through shared memory; when K is long the CTAs of one tile are combined by the last to
 // arrive, in ascending split order.  Every order is fixed, so replays are bit-identical.
+//
+// RMS-norm variant (q8_0_gemv_rms): the same page's down kernel stages R' * w_norm unscaled with
+// the rows' sums of squares, and the last work-group to arrive applies rs per stream.  Here each
+// lane multiplies its activations by the norm weight g as it loads them (bf16 x bf16 is exact in
+// fp32, rounded once to bf16 for the MMA) and sums their squares in fp32; the squares travel with
+// the dot products through every combine (warp order, the cluster, ascending splits) and the final
+// store scales row t by rs[t] = 1 / sqrt(sum_k x[t,k]^2 / K + eps), all IEEE operations.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -22,12 +29,17 @@ namespace w8a8 {
 constexpr int kQ8MaxWarps = 16;
 constexpr int kQ8MaxBlocksPerWarp = 8;
 constexpr int kQ8TargetBlocksPerWarp = 4;
+// float4 per (tile, split) record of a split read: 32 lanes' partial sums, then the 8 rows' sums
+// of squares (RMS-norm variant).
+constexpr int kQ8Rec = 34;
 // One CTA covers up to 16 warps x 8 blocks = 4096 k of a tile, so K <= 4096 needs no cross-CTA
 // combine: its two dependent global round trips (counter, then the partials) cost more than the
 // extra loads each warp keeps in flight.
 
 struct Q8Params {
   const uint16_t* x;
+  const uint16_t* gamma;   // RMS-norm variant: the norm weight g [K] (bf16)
+  float eps;
   const int8_t* q;
   const uint16_t* d;
   uint16_t* y;
@@ -49,6 +61,16 @@ __device__ __forceinline__ uint32_t s8x2_to_bf16x2(uint32_t u, int i0, int i1) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// 32-bit store into another CTA's shared memory (shared::cluster address).
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// rs = 1 / sqrt(ss / K + eps), each step one IEEE operation.
+__device__ __forceinline__ float inv_rms(float ss, int K, float eps) {
+  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)K), eps)));
+}
+
 __device__ __forceinline__ void q8_store(const Q8Params& p, const float (&v)[4], int n_a, int c) {
   const int n_b = n_a + 8;
 #pragma unroll
@@ -59,8 +81,10 @@ __device__ __forceinline__ void q8_store(const Q8Params& p, const float (&v)[4],
   }
 }
 
+template <bool kRms>
 __global__ void __launch_bounds__(32 * kQ8MaxWarps) q8_0_gemv_kernel(const __grid_constant__ Q8Params p) {
   __shared__ float4 red[kQ8MaxWarps][32];
+  __shared__ float ssred[kQ8MaxWarps][8];   // RMS-norm variant: each warp's sums of squares per row
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int rank = p.cluster > 1 ? (int)cluster_ctarank() : 0;
@@ -81,7 +105,7 @@ __global__ void __launch_bounds__(32 * kQ8MaxWarps) q8_0_gemv_kernel(const __gri
   // The quants and scales are weights (never written by the work this call depends on), so they
   // are requested before the dependency wait; the activations after it.
   uint2 qa[kQ8MaxBlocksPerWarp], qb[kQ8MaxBlocksPerWarp];
-  uint4 xv[kQ8MaxBlocksPerWarp];
+  uint4 xv[kQ8MaxBlocksPerWarp], gv[kQ8MaxBlocksPerWarp];
   uint16_t da[kQ8MaxBlocksPerWarp], db[kQ8MaxBlocksPerWarp];
 #pragma unroll
   for (int i = 0; i < kQ8MaxBlocksPerWarp; ++i) {
@@ -101,6 +125,9 @@ __global__ void __launch_bounds__(32 * kQ8MaxWarps) q8_0_gemv_kernel(const __gri
         db[i] = __ldg(p.d + (long long)n_b * p.KB + kb);
       }
     }
+    // The norm weight is a weight too: fetched before the dependency wait.
+    if (kRms) gv[i] = i < nb ? __ldg(reinterpret_cast<const uint4*>(p.gamma + (long long)(wb0 + i) * 32 + 8 * c))
+                             : make_uint4(0u, 0u, 0u, 0u);
   }
   pdl_wait();
 #pragma unroll
@@ -108,6 +135,32 @@ __global__ void __launch_bounds__(32 * kQ8MaxWarps) q8_0_gemv_kernel(const __gri
     xv[i] = make_uint4(0u, 0u, 0u, 0u);
     if (i < nb && g < p.T)
       xv[i] = __ldcg(reinterpret_cast<const uint4*>(p.x + (long long)g * p.K + (long long)(wb0 + i) * 32 + 8 * c));
+  }
+  // RMS-norm variant: this lane's sum of x^2 (blocks ascending, elements in order; each square is
+  // exact in fp32) and its activations times g, rounded once to bf16.  The four lanes of a row
+  // then add their sums (same bits in all four).
+  float ss = 0.f;
+  if (kRms) {
+#pragma unroll
+    for (int i = 0; i < kQ8MaxBlocksPerWarp; ++i) {
+      if (i < nb) {
+        const uint32_t xw[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+        const uint32_t gw[4] = {gv[i].x, gv[i].y, gv[i].z, gv[i].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float x0 = __uint_as_float(xw[e] << 16), x1 = __uint_as_float(xw[e] & 0xFFFF0000u);
+          const float g0 = __uint_as_float(gw[e] << 16), g1 = __uint_as_float(gw[e] & 0xFFFF0000u);
+          ss = __fadd_rn(ss, __fmul_rn(x0, x0));
+          ss = __fadd_rn(ss, __fmul_rn(x1, x1));
+          __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(x0, g0), __fmul_rn(x1, g1));
+          o[e] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        xv[i] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+    ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, 1));
+    ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, 2));
   }
 
   // One independent 16x8 block product per 32-k block (two k16 MMAs each, all step-0 MMAs issued
@@ -152,29 +205,46 @@ __global__ void __launch_bounds__(32 * kQ8MaxWarps) q8_0_gemv_kernel(const __gri
   if (p.cluster > 1) {
     // The tile's warp partials gather in CTA 0 of the cluster (distributed shared memory), which
     // sums them in warp order, exactly as one CTA holding all the tile's warps would.
-    if (tw < p.tile_warps)
+    if (tw < p.tile_warps) {
       st_cluster_v4f(cluster_map(smem_addr(&red[tw][lane]), 0u), make_float4(acc[0], acc[1], acc[2], acc[3]));
+      if (kRms && c == 0) st_cluster_f32(cluster_map(smem_addr(&ssred[tw][g]), 0u), ss);
+    }
     cluster_sync_all();
     if (rank != 0 || warp != 0) return;
   } else {
     red[warp][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    if (kRms && c == 0) ssred[warp][g] = ss;
     __syncthreads();
     if (warp != 0) return;
   }
+  // This lane stores rows t = 2c and 2c + 1: their sums of squares, in warp order too.
   float tot[4] = {0.f, 0.f, 0.f, 0.f};
+  float ts0 = 0.f, ts1 = 0.f;
   for (int w = 0; w < p.tile_warps; ++w) {
     const float4 v = red[w][lane];
     tot[0] += v.x;
     tot[1] += v.y;
     tot[2] += v.z;
     tot[3] += v.w;
+    if (kRms) {
+      ts0 = __fadd_rn(ts0, ssred[w][2 * c]);
+      ts1 = __fadd_rn(ts1, ssred[w][2 * c + 1]);
+    }
   }
   if (p.splits == 1) {
+    if (kRms) {
+      const float r0 = inv_rms(ts0, p.K, p.eps), r1 = inv_rms(ts1, p.K, p.eps);
+      tot[0] = __fmul_rn(tot[0], r0);
+      tot[1] = __fmul_rn(tot[1], r1);
+      tot[2] = __fmul_rn(tot[2], r0);
+      tot[3] = __fmul_rn(tot[3], r1);
+    }
     q8_store(p, tot, n_a, c);
     return;
   }
-  float4* mine = p.partials + ((long long)tile * p.splits + split) * 32;
+  float4* mine = p.partials + ((long long)tile * p.splits + split) * kQ8Rec;
   __stcg(mine + lane, make_float4(tot[0], tot[1], tot[2], tot[3]));
+  if (kRms && lane < 4) __stcg(reinterpret_cast<float2*>(mine + 32) + lane, make_float2(ts0, ts1));
   __threadfence();
   __syncwarp();
   uint32_t old = 0;
@@ -188,13 +258,20 @@ __global__ void __launch_bounds__(32 * kQ8MaxWarps) q8_0_gemv_kernel(const __gri
   __threadfence();
   // Ascending split order; each batch's loads are all in flight before the first is used.
   float sum[4] = {0.f, 0.f, 0.f, 0.f};
+  float ssum0 = 0.f, ssum1 = 0.f;
   for (int base = 0; base < p.splits; base += 8) {
     float4 v[8];
+    float2 sv[8];
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
       const int s = base + b;
       v[b] = make_float4(tot[0], tot[1], tot[2], tot[3]);
-      if (s < p.splits && s != split) v[b] = __ldcg(p.partials + ((long long)tile * p.splits + s) * 32 + lane);
+      sv[b] = make_float2(ts0, ts1);
+      if (s < p.splits && s != split) {
+        const float4* rec = p.partials + ((long long)tile * p.splits + s) * kQ8Rec;
+        v[b] = __ldcg(rec + lane);
+        if (kRms) sv[b] = __ldcg(reinterpret_cast<const float2*>(rec + 32) + c);
+      }
     }
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
@@ -203,10 +280,21 @@ __global__ void __launch_bounds__(32 * kQ8MaxWarps) q8_0_gemv_kernel(const __gri
         sum[1] += v[b].y;
         sum[2] += v[b].z;
         sum[3] += v[b].w;
+        if (kRms) {
+          ssum0 = __fadd_rn(ssum0, sv[b].x);
+          ssum1 = __fadd_rn(ssum1, sv[b].y);
+        }
       }
     }
   }
   if (lane == 0) atomicExch(p.counters + tile, 0u);
+  if (kRms) {
+    const float r0 = inv_rms(ssum0, p.K, p.eps), r1 = inv_rms(ssum1, p.K, p.eps);
+    sum[0] = __fmul_rn(sum[0], r0);
+    sum[1] = __fmul_rn(sum[1], r1);
+    sum[2] = __fmul_rn(sum[2], r0);
+    sum[3] = __fmul_rn(sum[3], r1);
+  }
   q8_store(p, sum, n_a, c);
 }
 
@@ -232,7 +320,7 @@ int q8_plan(int T, int K, int N, Q8Plan* plan) {
   }
   pl.blocks = pl.n_tiles * pl.splits * pl.cluster;
   const size_t counters = ((size_t)pl.n_tiles * 4 + 255) / 256 * 256;
-  const size_t partials = pl.splits > 1 ? (size_t)pl.n_tiles * pl.splits * 32 * 16 : 0;
+  const size_t partials = pl.splits > 1 ? (size_t)pl.n_tiles * pl.splits * kQ8Rec * 16 : 0;
   pl.counters_offset = kWsHeaderBytes;
   pl.partials_offset = kWsHeaderBytes + counters;
   pl.workspace_bytes = kWsHeaderBytes + counters + partials;
@@ -241,9 +329,11 @@ int q8_plan(int T, int K, int N, Q8Plan* plan) {
 }
 
 cudaError_t q8_launch(const Q8Plan& pl, const void* x, const int8_t* q, const void* d, void* y, int T, int K, int N,
-                      void* ws, bool pdl, cudaStream_t stream) {
+                      void* ws, bool pdl, cudaStream_t stream, const void* gamma, float eps) {
   Q8Params p;
   p.x = static_cast<const uint16_t*>(x);
+  p.gamma = static_cast<const uint16_t*>(gamma);
+  p.eps = eps;
   p.q = q;
   p.d = static_cast<const uint16_t*>(d);
   p.y = static_cast<uint16_t*>(y);
@@ -279,7 +369,7 @@ cudaError_t q8_launch(const Q8Plan& pl, const void* x, const int8_t* q, const vo
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, q8_0_gemv_kernel, p);
+  cudaError_t e = gamma ? cudaLaunchKernelEx(&cfg, q8_0_gemv_kernel<true>, p) : cudaLaunchKernelEx(&cfg, q8_0_gemv_kernel<false>, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

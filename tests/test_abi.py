@@ -283,6 +283,23 @@ def test_quantisation_entry_points_check_arguments_on_the_host():
     assert L.q8_0_blocks_from_split(a, a, a, 4096, 0, None) == 1
 
 
+def test_rms_read_checks_its_arguments_on_the_host():
+    L = lib8.lib()
+    a = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    qws = lib8.q8_0_workspace_bytes(6, 4096, 320)
+    f = ctypes.c_float
+    assert L.q8_0_gemv_rms(a, None, f(1e-6), a, a, a, 6, 4096, 320, 0, a, qws, None) == 1      # no gamma
+    assert L.q8_0_gemv_rms(a, a, f(-1.0), a, a, a, 6, 4096, 320, 0, a, qws, None) == 1        # eps < 0
+    assert L.q8_0_gemv_rms(a, a, f(float("nan")), a, a, a, 6, 4096, 320, 0, a, qws, None) == 1
+    assert L.q8_0_gemv_rms(a, a, f(float("inf")), a, a, a, 6, 4096, 320, 0, a, qws, None) == 1
+    assert L.q8_0_gemv_rms(a, odd, f(1e-6), a, a, a, 6, 4096, 320, 0, a, qws, None) == 3      # gamma misaligned
+    assert L.q8_0_gemv_rms(a, a, f(1e-6), a, a, a, 6, 4096, 320, 0, a, qws - 1, None) == 4
+    assert L.q8_0_gemv_rms(a, a, f(1e-6), a, a, a, 9, 4096, 320, 0, a, qws, None) == 1        # T > 8
+    assert L.q8_0_gemv_rms(a, a, f(1e-6), a, a, a, 6, 4016, 320, 0, a, qws, None) == 2        # K % 32
+    assert L.q8_0_gemv_rms(a, a, f(1e-6), a, a, a, 6, 4096, 320, 2, a, qws, None) == 1        # unknown flag
+
+
 def test_calls_with_null_pointers_fail_before_any_launch():
     L = lib8.lib()
     null = ctypes.c_void_p(0)

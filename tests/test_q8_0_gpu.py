@@ -103,8 +103,9 @@ def test_the_quantised_bytes_are_read():
 def test_counters_reset_after_split_calls():
     c = Q8Case(6, 8192, 320, seed=1)      # 256 k-blocks: two CTAs per tile, combined by the last
     n_tiles = (320 + 15) // 16
-    # the split layout's partials are in the workspace: 2 splits x 32 lanes x 16 bytes per tile
-    assert lib8.q8_0_workspace_bytes(6, 8192, 320) == 256 + 256 + n_tiles * 2 * 32 * 16
+    # the split layout's partials are in the workspace: per tile 2 splits x (32 lanes x 16 bytes of
+    # sums + 32 bytes of the 8 rows' sums of squares, used by the RMS-norm variant)
+    assert lib8.q8_0_workspace_bytes(6, 8192, 320) == 256 + 256 + n_tiles * 2 * 34 * 16
     for _ in range(3):
         _check(c)
     n_tiles = (320 + 15) // 16
