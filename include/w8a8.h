@@ -14,6 +14,8 @@
  *              fp16 scale each), T <= 8, bf16 out.  Defined by "sycl: STRATA_HC_Q8=1 reads the Q8_0
  *              hyper-connection projections", section "What changed" (w = d * q, the split layout,
  *              fixed-order partial sums, last work-group combine).
+ *  q8_0_gemv_rms  the same read with an RMS-norm prologue: y = rs[t] * (x * gamma) @ w (same page,
+ *              same section: the down kernel's R' * w_norm staging with the sums of squares).
  *
  * Conventions for every entry point:
  *  - Data pointers are DEVICE pointers (cudaMalloc or equivalent) unless stated otherwise; the
