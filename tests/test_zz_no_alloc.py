@@ -32,7 +32,9 @@ def _no_alloc(case, out, blocks=0, flags=0):
                                          case.M, case.K, case.N, blocks, flags, stream)
 
 
-@pytest.mark.parametrize("M,K,N,blocks", [(16, 4096, 1536, 0), (5, 512, 200, 7), (32, 2048, 4096, 0)])
+# M > 32 runs the tensor-memory arm (two launches; its scratch holds the fp16 activations too).
+@pytest.mark.parametrize("M,K,N,blocks", [(16, 4096, 1536, 0), (5, 512, 200, 7), (32, 2048, 4096, 0),
+                                          (64, 4096, 1536, 0), (100, 2048, 384, 7), (128, 2048, 4096, 0)])
 def test_no_alloc_matches_workspace_entry_point_twice(M, K, N, blocks):
     x, xs, W, ws = synth.w8a8_inputs(M, K, N, seed=M + K + N)
     case = W8A8Case(x, xs, W, ws, blocks=blocks)
