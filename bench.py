@@ -8,6 +8,10 @@ HBM (inputs larger than L2; no flush needed).  One step = one CUDA-graph replay 
 through the R buffers.  W warm-up steps, then K timed steps bracketed by a barrier and a device
 synchronise, timed with CUDA events on the launching stream; max over ranks.
 
+Beside the headline the line reports the same call launched with PDL, an end-to-end leg with host
+buffers, the Q8_0 reads (plain and RMS-norm), the quantisation rows, the 32 < M <= 128 arm at
+M = 128 (tensor_memory_arm), the read ceiling and the oracle's CPU baseline.
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--sweep]
 Under torchrun each rank runs an independent replica (the operator has no exchange step).
 """
