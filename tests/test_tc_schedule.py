@@ -7,7 +7,8 @@ own.  This test runs the roles' programs, with the slot, phase and period arithm
 way the kernel computes it, under random interleavings and random MMA completion delays, for the
 CTA runs the library's own split plans produce, and checks that
 
-  * every wait finds its barrier at the needed phase or one short of it (no aliasing),
+  * every wait checks its barrier with the phase it names, or the one before, completed last (the
+    parity of an older phase would pass early; two phases on it would block on a phase long gone),
   * no slot is overwritten or read before the role that owns it has finished with it (the weight,
     activation and tensor-memory A rings, the accumulator buffers and their read-out),
   * every role finishes (no deadlock), and
@@ -23,6 +24,7 @@ import random
 import pytest
 
 import int8_weight_gemm_gb300 as lib8
+from schedule_util import Barrier, run_roles, wait
 
 STAGE_UNITS = 4
 PERIOD_STAGES = 4
@@ -78,27 +80,6 @@ class Walk:
             self.ns = min(STAGE_UNITS, self.seg_end - self.u)
 
 
-class Barrier:
-    def __init__(self, name, count):
-        self.name, self.count = name, count
-        self.pending = count
-        self.completed = 0
-
-    def arrive(self):
-        self.pending -= 1
-        assert self.pending >= 0, f"{self.name}: more arrivals than its count"
-        if self.pending == 0:
-            self.completed += 1
-            self.pending = self.count
-
-    def ready(self, parity, target):
-        """A wait for completion index `target` (0-based), asked by parity as the kernel does."""
-        assert parity == target & 1, f"{self.name}: parity {parity} does not name completion {target}"
-        assert self.completed <= target + 1, \
-            f"{self.name}: completion {target} waited for after {self.completed} completions (aliasing)"
-        return self.completed == target + 1
-
-
 def _run_cta(b0, b1, KB, n_mma, seed):
     rng = random.Random(seed)
     NW, NB, NA, kI = (10, 4, 4, 2) if n_mma == 64 else (8, 3, 3, 1)
@@ -114,10 +95,6 @@ def _run_cta(b0, b1, KB, n_mma, seed):
     pending_commits = [[] for _ in range(kI)]   # per issuer, in issue order: barriers to arrive on
     log = {"converted": [], "issued": [[] for _ in range(kI)], "retired": [[] for _ in range(C)],
            "drained": [[] for _ in range(C)]}
-
-    def wait(bar, parity, target):
-        while not bar.ready(parity, target):
-            yield
 
     def w_producer():
         it, q = Walk(b0, b1, KB), 0
@@ -222,18 +199,7 @@ def _run_cta(b0, b1, KB, n_mma, seed):
 
     roles = [w_producer(), b_producer(), mma_engine()] + [issuer_wrapped(i) for i in range(kI)] + \
             [converter(w) for w in range(C)]
-    live = list(range(len(roles)))
-    idle = 0
-    while live:
-        k = rng.choice(live)
-        try:
-            next(roles[k])
-        except StopIteration:
-            live.remove(k)
-            idle = 0
-            continue
-        idle += 1
-        assert idle < 200000, "deadlock: no role finishes"
+    run_roles(roles, seed + 1)
     walk = Walk(b0, b1, KB)
     stages = periods = 0
     while not walk.done():
