@@ -226,9 +226,8 @@ __device__ __forceinline__ bool mbar_wait_lane0(uint64_t* bar, uint32_t parity, 
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// One arrival for the warp, after every lane's earlier work (the warp barrier orders it).  Barriers
-// the converter warps signal count warps, not threads: 512 arrivals on one shared-memory word per
-// stage were measured to cost more than the stage's work.
+// One arrival for the warp, after every lane's earlier work (the warp barrier orders it): the
+// barriers the converter warps signal count warps, not threads.
 __device__ __forceinline__ void mbar_arrive_warp(uint64_t* bar) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
