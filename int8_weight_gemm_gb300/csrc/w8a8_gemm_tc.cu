@@ -36,8 +36,9 @@
 //      (64 k x N_mma rows each, 128-byte swizzle: the MMA's B operand as it lands) into a short
 //      ring that the MMAs free;
 //    - sixteen converter warps: the weight rows go into tensor memory as the fp16 A operand
-//      (tcgen05.st, lane = row, one packed 16-byte chunk per thread and store).  The same warps retire each stage once its MMAs have completed
-//      (they wait for that anyway before reusing its tensor-memory slot): at the end of a period
+//      (tcgen05.st, lane = row, one packed 16-byte chunk per thread and store).  The same warps
+//      retire each stage once its MMAs have completed (they wait for that anyway before reusing
+//      its tensor-memory slot): at the end of a period
 //      they read the accumulators out and keep int32 sums in registers (each warp one lane
 //      quarter and one quarter of the columns), and at the end of a segment they store bf16 or
 //      add the split tile's partial and, as the last arrival, finish it;
@@ -179,8 +180,9 @@ __device__ __forceinline__ uint16_t epilogue(int acc, float xsv, float wsv) {
 }
 
 // Bounded wait for the phase of `parity` that polls with the non-blocking mbarrier.test_wait.  Every
-// role of this kernel blocks on a barrier once or more per stage, and a thread suspended in
-// mbarrier.try_wait was measured to resume well after the phase completes, so these waits poll;
+// role of this kernel blocks on a barrier once or more per stage, and the same kernel with its
+// waits suspended in mbarrier.try_wait was measured slower (gate_up-sized 90 us against 68 us
+// polling), so these waits poll;
 // a short sleep between polls keeps the polling warps from taking the issue slots that the
 // working warps (above all the MMA-issuing thread) need.  Gives up when another thread has
 // raised *abort, or after kWaitTimeoutCycles (then records the timeout in *status and raises
