@@ -29,17 +29,17 @@ void record_error(const char* text) { std::snprintf(g_last_error, sizeof(g_last_
 
 static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Number of SMs of the current device; 152 (GB300) when no device can be queried, so that the
-// host-only plan queries answer the same way on a machine without a GPU.
-static int current_sm_count() {
+// The GB300 count when no device can be queried, so that the host-only plan queries answer the
+// same way on a machine without a GPU.
+int device_sm_count() {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
-    return 152;
+    return kDefaultSmCount;
   }
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
     cudaGetLastError();
-    return 152;
+    return kDefaultSmCount;
   }
   return sms;
 }
@@ -147,7 +147,7 @@ size_t w8a8_packed_weight_bytes(int K, int N) {
 
 size_t w8a8_workspace_bytes(int M_max, int K, int N, int blocks) {
   if (M_max < 1 || M_max > kTcMaxM) return 0;
-  const int sms = current_sm_count();
+  const int sms = device_sm_count();
   size_t best = 0;
   // One plan per kernel variant that some M in [1, M_max] runs: the decode arm's n8-tile counts,
   // then the tensor-memory arm's two MMA widths.
@@ -166,7 +166,7 @@ size_t w8a8_workspace_bytes(int M_max, int K, int N, int blocks) {
 int w8a8_plan(int M, int K, int N, int blocks, w8a8_plan_t* plan) {
   if (!plan) return W8A8_ERR_INVALID_ARG;
   AnyPlan ap;
-  int rc = any_plan(M, K, N, blocks, current_sm_count(), &ap);
+  int rc = any_plan(M, K, N, blocks, device_sm_count(), &ap);
   if (rc != W8A8_OK) return rc;
   if (ap.tc) {
     const TcPlan& pl = ap.t;
@@ -205,7 +205,7 @@ int w8a8_plan(int M, int K, int N, int blocks, w8a8_plan_t* plan) {
 int w8a8_split_bounds_m(int M, int K, int N, int blocks, long long* bounds, int n_bounds) {
   if (!bounds) return W8A8_ERR_INVALID_ARG;
   AnyPlan ap;
-  int rc = any_plan(M, K, N, blocks, current_sm_count(), &ap);
+  int rc = any_plan(M, K, N, blocks, device_sm_count(), &ap);
   if (rc != W8A8_OK) return rc;
   const int n_tiles = ap.tc ? ap.t.n_tiles : ap.g.n_tiles;
   const int kb = ap.tc ? ap.t.kb : ap.g.kb;
@@ -244,7 +244,7 @@ int w8a8_gemm(const int8_t* x_q, const float* x_scale, const void* W_packed, con
   if (!x_q || !x_scale || !W_packed || !w_scale || !out || !ws) return W8A8_ERR_INVALID_ARG;
   if (flags & ~(unsigned)W8A8_FLAG_PDL) return W8A8_ERR_INVALID_ARG;
   AnyPlan pl;
-  int rc = any_plan(M, K, N, blocks, current_sm_count(), &pl);
+  int rc = any_plan(M, K, N, blocks, device_sm_count(), &pl);
   if (rc != W8A8_OK) return rc;
   if (!aligned(x_q, 16) || !aligned(W_packed, 16) || !aligned(out, 16) || !aligned(x_scale, 4) ||
       !aligned(w_scale, 4) || !aligned(ws, 256))

@@ -11,6 +11,12 @@ namespace w8a8 {
 // Every workspace starts with this header; its first 32-bit word is the device status.
 constexpr size_t kWsHeaderBytes = 256;
 
+// SMs of a GB300, the count assumed when no device can be queried (host-only plan queries).
+constexpr int kDefaultSmCount = 152;
+
+// Number of SMs of the current device, else kDefaultSmCount; clears any error the query raised.
+int device_sm_count();
+
 struct GemmPlan {
   int nt8, n_tiles, kb;
   long long slabs;

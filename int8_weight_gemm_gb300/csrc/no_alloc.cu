@@ -53,11 +53,7 @@ extern "C" int w8a8_gemm_no_alloc(const int8_t* x_q, const float* x_scale, const
                                   unsigned flags, void* stream) {
   if (!x_q || !x_scale || !W_packed || !w_scale || !out) return W8A8_ERR_INVALID_ARG;
   if (flags & ~(unsigned)W8A8_FLAG_PDL) return W8A8_ERR_INVALID_ARG;
-  int dev = 0, sms = 152;
-  if (cudaGetDevice(&dev) == cudaSuccess) {
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
-  }
-  cudaGetLastError();
+  const int sms = device_sm_count();
   AnyPlan pl;
   const int rc = any_plan(M, K, N, blocks, sms, &pl);
   if (rc != W8A8_OK) return rc;

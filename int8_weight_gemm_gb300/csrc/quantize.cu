@@ -143,7 +143,8 @@ __global__ void __launch_bounds__(256) q8_0_blocks_from_split_kernel(const uint4
 
 static unsigned grid_for(long long items, int threads) {
   long long g = (items + threads - 1) / threads;
-  if (g > 8 * 152 * 8) g = 8 * 152 * 8;   // grid-stride beyond a few waves
+  const long long cap = 64LL * kDefaultSmCount;   // grid-stride beyond a few waves
+  if (g > cap) g = cap;
   return (unsigned)(g < 1 ? 1 : g);
 }
 

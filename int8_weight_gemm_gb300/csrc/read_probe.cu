@@ -36,11 +36,7 @@ using namespace w8a8;
 extern "C" int w8a8_read_probe(const void* buf, size_t bytes, void* sink, void* stream) {
   if (!buf || !sink || bytes < 16) return W8A8_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(buf) & 15u) || (reinterpret_cast<uintptr_t>(sink) & 7u)) return W8A8_ERR_MISALIGNED;
-  int dev = 0, sms = 152;
-  if (cudaGetDevice(&dev) == cudaSuccess) {
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
-  }
-  cudaGetLastError();
+  const int sms = device_sm_count();
   // Two 512-thread CTAs per SM: 32 warps per SM, each with four 16-byte loads per lane in flight.
   read_probe_kernel<<<2 * sms, 512, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4*>(buf), bytes / 16, static_cast<unsigned long long*>(sink));

@@ -612,7 +612,7 @@ static cudaError_t launch_tc(const TcParams& p, int blocks, cudaStream_t stream)
 
 static cudaError_t launch_x16(const int8_t* x, void* x16, long long units, bool pdl, cudaStream_t stream) {
   long long grid = (units + 255) / 256;
-  if (grid > 8 * 152) grid = 8 * 152;
+  if (grid > 8 * kDefaultSmCount) grid = 8 * kDefaultSmCount;   // grid-stride beyond a few waves
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(grid < 1 ? 1 : grid));
   cfg.blockDim = dim3(256);
@@ -645,7 +645,7 @@ int tc_plan(int M, int K, int N, int blocks, int sm_count, TcPlan* plan) {
     // every CTA whole tiles, so no tile needs a combine; at M = 128 a tile's partial sums are as
     // large as 512 k of its weight, and such a plan was measured faster (gate_up-sized, 192
     // tiles: 96 CTAs 68 us, 152 CTAs 102 us).  Otherwise one CTA per SM.
-    const int sms = sm_count > 0 ? sm_count : 152;
+    const int sms = sm_count > 0 ? sm_count : kDefaultSmCount;
     long long g = sms;
     if (pl.n_tiles >= sms) {
       for (int c = sms; 2 * c >= sms; --c) {
