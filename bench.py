@@ -67,6 +67,12 @@ def whole_job_gbs(world: int, bytes_per_call: int, calls_per_rank: int, total_ms
     return world * bytes_per_call * calls_per_rank / (total_ms_max / 1e3) / 1e9
 
 
+def p90(sorted_values):
+    """Nearest-rank 90th percentile of an ascending list: the smallest value with at least 90 % of
+    the samples at or below it (never below the median)."""
+    return sorted_values[max(0, math.ceil(0.9 * len(sorted_values)) - 1)]
+
+
 def _env_int(name, default):
     try:
         return int(os.environ.get(name, default))
@@ -256,7 +262,7 @@ def time_gemm(M, K, N, dist, seed, steps, warmup, blocks=0, device=None, sample_
                    f"w8a8_gemm_kernel<{plan['n8_tiles']}, {plan['stages']}, {str(plan['threads'] == 320).lower()}>"),
         "blocks": plan["blocks"],
         "us_median": statistics.median(per_call_us),
-        "us_p90": per_call_us[min(len(per_call_us) - 1, int(0.9 * len(per_call_us)))],
+        "us_p90": p90(per_call_us),
         "avg_launch_us": total_ms * 1e3 / (steps * C),
         "clocks": clocks,
         "launches": steps * C,
@@ -489,7 +495,7 @@ def time_q8(T, K, N, iters=200, seed=7, flags=0, rms=False):
         samples.append(a.elapsed_time(b) * 1e3 / R)
     samples.sort()
     return {"T": T, "K": K, "N": N, "flags": flags, "rms_norm": rms, "us_median": statistics.median(samples),
-            "us_p90": samples[int(0.9 * (len(samples) - 1))], "weight_bytes": nbytes,
+            "us_p90": p90(samples), "weight_bytes": nbytes,
             "GBps": nbytes / statistics.median(samples) / 1e3}
 
 
@@ -624,7 +630,7 @@ def run_reference(args):
         "config": {"workload": f"W8A8 GEMM M={M}, K={K}, N={N} (fused-QKV-like decode shape)", "M": M, "K": K,
                    "N": N, "sample_columns": cols},
         "us_per_call": {"median": round(statistics.median(times) * 1e6, 1),
-                        "p90": round(times[int(0.9 * (len(times) - 1))] * 1e6, 1)},
+                        "p90": round(p90(times) * 1e6, 1)},
         "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": sample, "value": round(value, 4), "unit": "GB/s"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,

@@ -1,0 +1,48 @@
+"""The bench's host-side reporting on the CPU: the percentile it reports and the reference arm's
+JSON line (the oracle timed on the host, rank 0 of a single process)."""
+import json
+import os
+import random
+import statistics
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_p90_is_the_nearest_rank_and_never_below_the_median():
+    assert bench.p90([5.0]) == 5.0
+    assert bench.p90([1.0, 2.0]) == 2.0
+    assert bench.p90(list(range(10))) == 8          # 9 of 10 samples at or below it
+    assert bench.p90(list(range(100))) == 89
+    rng = random.Random(3)
+    for n in range(1, 60):
+        xs = sorted(rng.random() for _ in range(n))
+        v = bench.p90(xs)
+        assert v >= statistics.median(xs)
+        assert sum(x <= v for x in xs) >= 0.9 * n
+        assert sum(x < v for x in xs) < 0.9 * n
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "3",
+                        "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    out = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in out, key
+    assert out["impl"] == "reference" and out["metric"] == bench.METRIC
+    assert out["steps"] == 3 and out["warmup"] == 3 and out["n_gpus"] == 1
+    assert out["value"] > 0 and out["unit"] == "GB/s" and out["higher_is_better"] is True
+    assert out["us_per_call"]["p90"] >= out["us_per_call"]["median"] > 0
+    cb = out["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == out["value"] and cb["sample"]
+    assert out["e2e"] == {"value": out["value"], "unit": out["unit"], "h2d_bytes_per_step": 0,
+                          "d2h_bytes_per_step": 0}
+    assert out["config"]["workload"]
