@@ -2,12 +2,15 @@
 
 Argument marshalling only: every function forwards to the C ABI of the same name declared in
 include/w8a8.h, passing device pointers taken from torch tensors and the current CUDA stream.
+Since the C side sees bare pointers, the binding first checks each tensor it passes (contiguous,
+the element size the call reads, long enough, in CUDA memory) and raises ValueError otherwise.
 All arithmetic runs in the library's CUDA kernels; there is no fallback path, and a missing or
 unloadable library raises at the first call.
 """
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 
 from . import build as _build
@@ -144,12 +147,33 @@ def _nbytes(t):
     return t.numel() * t.element_size()
 
 
+def _dev(t, name, nbytes=0, esize=None):
+    """Layout check of a tensor whose pointer crosses the C ABI: contiguous, of element size
+    `esize` where the call reads the tensor's shape, and at least `nbytes` long (the C side sees a
+    bare pointer and cannot check).  Raises ValueError before any library call."""
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor (strides {tuple(t.stride())})")
+    if esize is not None and t.element_size() != esize:
+        raise ValueError(f"{name}: expected {esize}-byte elements, got {t.dtype}")
+    if nbytes and t.nbytes < nbytes:
+        raise ValueError(f"{name}: {t.nbytes} bytes, the call needs {nbytes}")
+
+
+def _on_cuda(**tensors):
+    """Every tensor of a call in CUDA memory (a host pointer handed to a kernel would fault):
+    checked after the layout checks, just before the library call."""
+    for name, t in tensors.items():
+        if t is not None and not t.is_cuda:
+            raise ValueError(f"{name}: expected a CUDA tensor, got device {t.device}")
+
+
 # ---------------------------------------------------------------------------------------------
 
 def w8a8_version() -> int:
     return lib().w8a8_version()
 
 
+@functools.lru_cache(maxsize=1024)
 def w8a8_packed_weight_bytes(K: int, N: int) -> int:
     return int(lib().w8a8_packed_weight_bytes(K, N))
 
@@ -179,10 +203,14 @@ def w8a8_split_bounds(K: int, N: int, blocks: int, M: int = 1) -> list:
 
 
 def w8a8_workspace_init(ws, stream=None) -> None:
+    _dev(ws, "ws")
+    _on_cuda(ws=ws)
     _check("w8a8_workspace_init", lib().w8a8_workspace_init(_ptr(ws), _nbytes(ws), _stream(stream)))
 
 
 def w8a8_workspace_status(ws, stream=None) -> int:
+    _dev(ws, "ws")
+    _on_cuda(ws=ws)
     v = ctypes.c_uint32(0)
     _check("w8a8_workspace_status", lib().w8a8_workspace_status(_ptr(ws), _nbytes(ws), _stream(stream), ctypes.byref(v)))
     return int(v.value)
@@ -203,8 +231,13 @@ def w8a8_pack_weights(W, W_packed=None, ws=None, stream=None):
     import torch
 
     K, N = W.shape
+    _dev(W, "W", esize=1)
     if W_packed is None:
         W_packed = torch.empty(w8a8_packed_weight_bytes(K, N), dtype=torch.uint8, device=W.device)
+    _dev(W_packed, "W_packed", w8a8_packed_weight_bytes(K, N))
+    if ws is not None:
+        _dev(ws, "ws")
+    _on_cuda(W=W, W_packed=W_packed, ws=ws)
     rc = lib().w8a8_pack_weights(_ptr(W), K, N, _ptr(W_packed), _ptr(ws), _nbytes(ws) if ws is not None else 0,
                                  _stream(stream))
     _check("w8a8_pack_weights", rc)
@@ -217,12 +250,28 @@ def w8a8_gemm(x_q, x_scale, W_packed, w_scale, ws, N: int, out=None, blocks: int
     import torch
 
     M, K = x_q.shape
+    _dev(x_q, "x_q", esize=1)
+    _dev(x_scale, "x_scale", 4 * M)
+    _dev(W_packed, "W_packed", w8a8_packed_weight_bytes(K, N))
+    _dev(w_scale, "w_scale", 4 * N)
+    _dev(ws, "ws")
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x_q.device)
+    _dev(out, "out", 2 * M * N)
+    _on_cuda(x_q=x_q, x_scale=x_scale, W_packed=W_packed, w_scale=w_scale, ws=ws, out=out)
     rc = lib().w8a8_gemm(_ptr(x_q), _ptr(x_scale), _ptr(W_packed), _ptr(w_scale), _ptr(out), M, K, N, blocks,
                          flags, _ptr(ws), _nbytes(ws), _stream(stream))
     _check("w8a8_gemm", rc)
     return out
+
+
+def _q8_args(x, q, d, ws, K, N):
+    _dev(x, "x", esize=2)
+    if q.dim() != 2 or q.shape[1] != K:
+        raise ValueError(f"q: expected shape [N, {K}], got {tuple(q.shape)}")
+    _dev(q, "q", esize=1)
+    _dev(d, "d", 2 * N * (K // 32))
+    _dev(ws, "ws")
 
 
 def q8_0_gemv(x, q, d, ws, y=None, flags: int = 0, stream=None):
@@ -231,8 +280,11 @@ def q8_0_gemv(x, q, d, ws, y=None, flags: int = 0, stream=None):
 
     T, K = x.shape
     N = q.shape[0]
+    _q8_args(x, q, d, ws, K, N)
     if y is None:
         y = torch.empty((T, N), dtype=torch.bfloat16, device=x.device)
+    _dev(y, "y", 2 * T * N)
+    _on_cuda(x=x, q=q, d=d, ws=ws, y=y)
     rc = lib().q8_0_gemv(_ptr(x), _ptr(q), _ptr(d), _ptr(y), T, K, N, flags, _ptr(ws), _nbytes(ws),
                          _stream(stream))
     _check("q8_0_gemv", rc)
@@ -245,8 +297,12 @@ def q8_0_gemv_rms(x, gamma, eps: float, q, d, ws, y=None, flags: int = 0, stream
 
     T, K = x.shape
     N = q.shape[0]
+    _q8_args(x, q, d, ws, K, N)
+    _dev(gamma, "gamma", 2 * K)
     if y is None:
         y = torch.empty((T, N), dtype=torch.bfloat16, device=x.device)
+    _dev(y, "y", 2 * T * N)
+    _on_cuda(x=x, gamma=gamma, q=q, d=d, ws=ws, y=y)
     rc = lib().q8_0_gemv_rms(_ptr(x), _ptr(gamma), float(eps), _ptr(q), _ptr(d), _ptr(y), T, K, N, flags, _ptr(ws),
                              _nbytes(ws), _stream(stream))
     _check("q8_0_gemv_rms", rc)
@@ -256,6 +312,9 @@ def q8_0_gemv_rms(x, gamma, eps: float, q, d, ws, y=None, flags: int = 0, stream
 def w8a8_read_probe(buf, sink, stream=None) -> None:
     """Read the whole device tensor `buf` once (16-byte loads) and discard it: the HBM read-rate
     probe.  `sink` is an 8-byte device tensor the kernel may write."""
+    _dev(buf, "buf")
+    _dev(sink, "sink", 8)
+    _on_cuda(buf=buf, sink=sink)
     _check("w8a8_read_probe", lib().w8a8_read_probe(_ptr(buf), _nbytes(buf), _ptr(sink), _stream(stream)))
 
 
@@ -264,10 +323,14 @@ def w8a8_quantize_activations(x, x_q=None, x_scale=None, stream=None):
     import torch
 
     M, K = x.shape
+    _dev(x, "x", esize=2)
     if x_q is None:
         x_q = torch.empty((M, K), dtype=torch.int8, device=x.device)
     if x_scale is None:
         x_scale = torch.empty(M, dtype=torch.float32, device=x.device)
+    _dev(x_q, "x_q", M * K)
+    _dev(x_scale, "x_scale", 4 * M)
+    _on_cuda(x=x, x_q=x_q, x_scale=x_scale)
     _check("w8a8_quantize_activations",
            lib().w8a8_quantize_activations(_ptr(x), _ptr(x_q), _ptr(x_scale), M, K, _stream(stream)))
     return x_q, x_scale
@@ -278,10 +341,14 @@ def q8_0_quantize(w, q=None, d=None, stream=None):
     import torch
 
     N, K = w.shape
+    _dev(w, "w", esize=2)
     if q is None:
         q = torch.empty((N, K), dtype=torch.int8, device=w.device)
     if d is None:
         d = torch.empty((N, K // 32), dtype=torch.int16, device=w.device)
+    _dev(q, "q", N * K)
+    _dev(d, "d", 2 * N * (K // 32))
+    _on_cuda(w=w, q=q, d=d)
     _check("q8_0_quantize", lib().q8_0_quantize(_ptr(w), _ptr(q), _ptr(d), K, N, _stream(stream)))
     return q, d
 
@@ -290,10 +357,14 @@ def q8_0_split_from_blocks(blocks, K: int, N: int, q=None, d=None, stream=None):
     """ggml Q8_0 blocks (uint8, N * K/32 * 34 bytes) -> (q [N, K] int8, d [N, K/32] int16 bits)."""
     import torch
 
+    _dev(blocks, "blocks", 34 * N * (K // 32))
     if q is None:
         q = torch.empty((N, K), dtype=torch.int8, device=blocks.device)
     if d is None:
         d = torch.empty((N, K // 32), dtype=torch.int16, device=blocks.device)
+    _dev(q, "q", N * K)
+    _dev(d, "d", 2 * N * (K // 32))
+    _on_cuda(blocks=blocks, q=q, d=d)
     _check("q8_0_split_from_blocks", lib().q8_0_split_from_blocks(_ptr(blocks), _ptr(q), _ptr(d), K, N, _stream(stream)))
     return q, d
 
@@ -303,7 +374,11 @@ def q8_0_blocks_from_split(q, d, blocks=None, stream=None):
     import torch
 
     N, K = q.shape
+    _dev(q, "q", esize=1)
+    _dev(d, "d", 2 * N * (K // 32))
     if blocks is None:
         blocks = torch.empty((N, K // 32, 34), dtype=torch.uint8, device=q.device)
+    _dev(blocks, "blocks", 34 * N * (K // 32))
+    _on_cuda(q=q, d=d, blocks=blocks)
     _check("q8_0_blocks_from_split", lib().q8_0_blocks_from_split(_ptr(q), _ptr(d), _ptr(blocks), K, N, _stream(stream)))
     return blocks
