@@ -29,9 +29,9 @@
  *  - A workspace is caller-owned device memory, at least 256-byte aligned, sized with the
  *    *_workspace_bytes queries and zeroed once with w8a8_workspace_init (outside any capture)
  *    before its first use.  Every call leaves it ready for the next one (each arrival counter is
- *    reset by the last arrival, and every accumulator returned to zero).  Calls that use the same workspace must not overlap in time
- *    (use one stream per workspace); one workspace may serve both operators in turn if it is
- *    sized for the larger of the two.
+ *    reset by the last arrival, and every accumulator returned to zero).  Calls that use the
+ *    same workspace must not overlap in time (use one stream per workspace); one workspace may
+ *    serve both operators in turn if it is sized for the larger of the two.
  *  - bf16 and fp16 values are passed as their 16-bit patterns (uint16_t storage).
  */
 #ifndef W8A8_GB300_H
@@ -176,7 +176,7 @@ typedef struct {
                               f > 0 = two elements per word in f-bit fields plus a 64 - 2f bit
                               arrival count (chosen when both fit; halves the atomics) */
     int tile_rows;         /* weight rows per tile: 64 (M <= 32) or 128 (M > 32) */
-    int tensor_memory;     /* 1: the tcgen05 arm (accumulators in tensor memory), 0: the decode arm */
+    int tensor_memory;     /* 1: the tcgen05 arm (accumulators in tensor memory), 0: decode arm */
 } w8a8_plan_t;
 
 int w8a8_plan(int M, int K, int N, int blocks, w8a8_plan_t* plan);
@@ -189,10 +189,10 @@ int w8a8_split_bounds(int K, int N, int blocks, long long* bounds, int n_bounds)
 /* The same for the plan of an M-row call (M > 32: units of 32 k of a 128-row tile). */
 int w8a8_split_bounds_m(int M, int K, int N, int blocks, long long* bounds, int n_bounds);
 
-/* W8A8 GEMM (both arms) that allocates nothing and takes no workspace.  The pages have no counterpart:
- * this entry point exists for callers that cannot provide device memory, such as a plugin that
- * sees only the input and output pointers its host engine hands it, or a request path that must
- * not call cudaMalloc (which can synchronise the device and stall other streams).
+/* W8A8 GEMM (both arms) that allocates nothing and takes no workspace.  The pages have no
+ * counterpart: this entry point exists for callers that cannot provide device memory, such as a
+ * plugin that sees only the input and output pointers its host engine hands it, or a request path
+ * that must not call cudaMalloc (which can synchronise the device and stall other streams).
  *
  * Arguments, limits, result and errors are those of w8a8_gemm, without ws / ws_bytes.  The
  * workspace is a 16 MiB area inside this library's device memory (a file-scope __device__ array,
@@ -214,6 +214,38 @@ int w8a8_gemm_no_alloc(const int8_t* x_q, const float* x_scale, const void* W_pa
  * ----------------------------------------------------------------------------------------- */
 
 /* Workspace bytes that q8_0_gemv needs for every T in [1, T_max] at (K, N). */
+size_t q8_0_workspace_bytes(int T_max, int K, int N);
+
+/* y[t][n] = bf16_rne( sum_k x[t][k] * (d[n][k/32] * q[n][k]) ), summed in fp32 in a fixed order
+ * (bit-identical across replays).
+ *
+ *  x   [T,K] bf16 row-major, 16-byte aligned.
+ *  q   [N,K] int8 row-major: the quants of the split layout, 16-byte aligned.
+ *  d   [N,K/32] fp16 row-major: the block scales of the split layout (scale of q[n][32b..32b+31]
+ *      is d[n][b]), 2-byte aligned.
+ *  y   [T,N] bf16 row-major, 2-byte aligned; rows t >= T are never written.
+ *  T in [1, 8]; K % 32 == 0, 32 <= K <= 65536; 1 <= N <= 1048576.
+ *  flags 0 or W8A8_FLAG_PDL; any other bit is INVALID_ARG.
+ *  Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, WORKSPACE_TOO_SMALL, CUDA. */
+int q8_0_gemv(const void* x, const int8_t* q, const void* d, void* y, int T, int K, int N,
+              unsigned flags, void* ws, size_t ws_bytes, void* stream);
+
+/* The Q8_0 read with an RMS-norm prologue:
+ *   y[t][n] = bf16_rne( rs[t] * sum_k bf16(x[t][k] * gamma[k]) * (d[n][k/32] * q[n][k]) ),
+ *   rs[t]   = 1 / sqrt(sum_k x[t][k]^2 / K + eps),
+ * the generic form of "sycl: STRATA_HC_Q8=1 reads the Q8_0 hyper-connection projections", section
+ * "What changed" (the down kernel stages R' * w_norm unscaled with the rows' sums of squares, and
+ * the last work-group to arrive applies rs per stream).  The product x * gamma is exact in fp32 and
+ * rounded once to bf16 (the MMA's operand); the sums of squares are fp32 in a fixed order; rs is
+ * IEEE division and square root.  Replays are bit-identical.
+ *  gamma  [K] bf16 (the norm weight), 16-byte aligned; read before the dependency wait under
+ *         W8A8_FLAG_PDL, like q and d (a weight).
+ *  eps    finite and >= 0, else INVALID_ARG.
+ *  Everything else, the workspace (q8_0_workspace_bytes) and the errors as q8_0_gemv. */
+int q8_0_gemv_rms(const void* x, const void* gamma, float eps, const int8_t* q, const void* d,
+                  void* y, int T, int K, int N, unsigned flags, void* ws, size_t ws_bytes,
+                  void* stream);
+
 /* ---------------------------------------------------------------------------------------------
  * Quantisation around the operators (outside the timed GEMM / read).  Sources: the Q8_0 page
  * ("sycl: STRATA_HC_Q8=1 reads the Q8_0 hyper-connection projections", section "What changed",
@@ -251,38 +283,6 @@ int q8_0_blocks_from_split(const int8_t* q, const void* d, void* blocks, int K, 
  * achievable HBM read rate, the ceiling for the weight stream.  buf 16-byte aligned, sink 8-byte
  * aligned.  Errors: INVALID_ARG, MISALIGNED, CUDA. */
 int w8a8_read_probe(const void* buf, size_t bytes, void* sink, void* stream);
-
-size_t q8_0_workspace_bytes(int T_max, int K, int N);
-
-/* y[t][n] = bf16_rne( sum_k x[t][k] * (d[n][k/32] * q[n][k]) ), summed in fp32 in a fixed order
- * (bit-identical across replays).
- *
- *  x   [T,K] bf16 row-major, 16-byte aligned.
- *  q   [N,K] int8 row-major: the quants of the split layout, 16-byte aligned.
- *  d   [N,K/32] fp16 row-major: the block scales of the split layout (scale of q[n][32b..32b+31]
- *      is d[n][b]), 2-byte aligned.
- *  y   [T,N] bf16 row-major, 2-byte aligned; rows t >= T are never written.
- *  T in [1, 8]; K % 32 == 0, 32 <= K <= 65536; 1 <= N <= 1048576.
- *  flags 0 or W8A8_FLAG_PDL; any other bit is INVALID_ARG.
- *  Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, WORKSPACE_TOO_SMALL, CUDA. */
-int q8_0_gemv(const void* x, const int8_t* q, const void* d, void* y, int T, int K, int N,
-              unsigned flags, void* ws, size_t ws_bytes, void* stream);
-
-/* The Q8_0 read with an RMS-norm prologue:
- *   y[t][n] = bf16_rne( rs[t] * sum_k bf16(x[t][k] * gamma[k]) * (d[n][k/32] * q[n][k]) ),
- *   rs[t]   = 1 / sqrt(sum_k x[t][k]^2 / K + eps),
- * the generic form of "sycl: STRATA_HC_Q8=1 reads the Q8_0 hyper-connection projections", section
- * "What changed" (the down kernel stages R' * w_norm unscaled with the rows' sums of squares, and
- * the last work-group to arrive applies rs per stream).  The product x * gamma is exact in fp32 and
- * rounded once to bf16 (the MMA's operand); the sums of squares are fp32 in a fixed order; rs is
- * IEEE division and square root.  Replays are bit-identical.
- *  gamma  [K] bf16 (the norm weight), 16-byte aligned; read before the dependency wait under
- *         W8A8_FLAG_PDL, like q and d (a weight).
- *  eps    finite and >= 0, else INVALID_ARG.
- *  Everything else, the workspace (q8_0_workspace_bytes) and the errors as q8_0_gemv. */
-int q8_0_gemv_rms(const void* x, const void* gamma, float eps, const int8_t* q, const void* d,
-                  void* y, int T, int K, int N, unsigned flags, void* ws, size_t ws_bytes,
-                  void* stream);
 
 #ifdef __cplusplus
 }
