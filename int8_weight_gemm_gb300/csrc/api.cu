@@ -1,6 +1,6 @@
 // C ABI of the library: argument checks, launch plans and error reporting.  Every check runs
-// before any launch; each compute entry point issues one kernel launch (two for w8a8_gemm with M > 32:
-// the fp16 activation copy, then the GEMM as its programmatic dependent) and nothing else.
+// before any launch; each compute entry point issues one kernel launch (two for w8a8_gemm with
+// M > 32: the fp16 activation copy, then the GEMM as its programmatic dependent) and nothing else.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>

@@ -1,8 +1,8 @@
 // w8a8_gemm_no_alloc: the W8A8 GEMM for callers that cannot allocate device memory.
 //
-// w8a8_gemm needs a caller-provided workspace (the split-tile accumulators).  Some callers have no way to provide one.  An inference plugin hosted inside
-// another engine sees only the input and output pointers the host engine hands it, with no access
-// to that engine's allocator.  A latency-critical request path may forbid cudaMalloc/cudaFree
+// w8a8_gemm needs a caller-provided workspace (the split-tile accumulators).  Some callers have
+// no way to provide one.  An inference plugin hosted inside another engine sees only the input and
+// output pointers the host engine hands it, with no access to that engine's allocator.  A latency-critical request path may forbid cudaMalloc/cudaFree
 // outright, because those calls can synchronise the device and stall every other stream.  For
 // them this entry point runs the same kernel on a scratch area that lives in this library's own
 // device memory: a file-scope __device__ array reserved when the library's module is loaded on a
