@@ -607,7 +607,7 @@ int gemm_plan(int M, int K, int N, int blocks, int sm_count, GemmPlan* plan) {
   if (blocks == 0) {
     // Two CTAs on every SM: measured fastest for every workload shape once the split-tile
     // combine costs one round trip (fewer CTAs stream slower and save little in the combine).
-    const long long g = (long long)kAutoCtasPerSm * (sm_count > 0 ? sm_count : kDefaultSmCount);
+    const long long g = (long long)kAutoCtasPerSm * (sm_count > 0 ? sm_count : 152);
     pl.blocks = (int)(g < pl.slabs ? g : pl.slabs);
   } else {
     if (blocks > pl.slabs) return W8A8_ERR_INVALID_ARG;
