@@ -18,7 +18,7 @@
  * Readings where the pages leave a step open (also listed in the design notes):
  *  - The W8A8 epilogue is (float(acc) * x_scale[m]) * w_scale[n], each step an IEEE fp32
  *    multiply rounded to nearest even, then rounded to nearest even into bfloat16.  The pages
- *    only say "scales ... bf16"; the order is the one the benchmark spec fixes.
+ *    only say "scales ... bf16"; the library's interface defines this order, x_scale first.
  *  - Q8_0 blocks run along K inside each weight row n; d has shape [N, K/32].
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -shared -fPIC (see build.py).
