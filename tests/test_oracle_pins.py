@@ -336,6 +336,22 @@ def test_pack_places_each_weight_once():
             assert t == n // 64 and kb == k // 32
 
 
+def test_pack_positions_golden():
+    # Byte positions worked out by hand from the documented layout (tests/golden): a weight moved
+    # to another byte of its slab, e.g. with the row and k halves of a chunk swapped, is caught.
+    for K, N, off, k, n in _read_golden("w8a8_pack_positions.txt"):
+        K, N, off = int(K), int(N), int(off)
+        if k == "pad":
+            p = oracle.w8a8_pack(np.full((K, N), 5, np.int8))
+            assert p[off] == 0x80
+            continue
+        W = np.zeros((K, N), np.int8)
+        W[int(k), int(n)] = -3
+        p = oracle.w8a8_pack(W)
+        assert np.nonzero(p != 0x80)[0].tolist() == [off]
+        assert p[off] == (0xFD ^ 0x80)                     # -3 in offset binary
+
+
 # --------------------------------------------------------------------------------------------
 # Quantisation rows (activation quantisation in front of W8A8; Q8_0 from BF16 at load)
 # --------------------------------------------------------------------------------------------
