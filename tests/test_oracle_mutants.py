@@ -56,6 +56,14 @@ MUTANTS = [
     ("f16 ties away from zero", "(rem == 0x1000u && (r & 1u))", "(rem == 0x1000u)", ["f16_from", "quantize"]),
     ("q8_0 quantize rounds half to even", "(int8_t)roundf(bf16_to_f32(blk[j]) / dd)", "(int8_t)rintf(bf16_to_f32(blk[j]) / dd)",
      ["quantize"]),
+    ("q8_0 quantize divides by the fp16 scale", "(int8_t)roundf(bf16_to_f32(blk[j]) / dd)",
+     "(int8_t)roundf(bf16_to_f32(blk[j]) / (float)oracle_f16_to_f64(d[(size_t)n * nb + b]))", ["quantize"]),
+    ("q8_0 quantize amax without the absolute value",
+     "const float a = fabsf(bf16_to_f32(blk[j]));", "const float a = bf16_to_f32(blk[j]);", ["quantize"]),
+    ("rms squares x * gamma", "double v = oracle_bf16_to_f64(x[(size_t)t * K + k]);\n            ss += v * v;",
+     "double v = oracle_bf16_to_f64(x[(size_t)t * K + k]) * oracle_bf16_to_f64(g[k]);\n            ss += v * v;",
+     ["rms"]),
+    ("f16 subnormal cut-off", "if (e < 102) return sign;", "if (e < 103) return sign;", ["f16_from", "quantize"]),
     ("activation scale over 128", "const float s = amax / 127.0f;", "const float s = amax / 128.0f;", ["quantize_rows"]),
     ("blocks scale byte order", "blk[0] = (uint8_t)(s & 0xFFu);\n            blk[1] = (uint8_t)(s >> 8);",
      "blk[1] = (uint8_t)(s & 0xFFu);\n            blk[0] = (uint8_t)(s >> 8);", ["inverse", "blocks"]),
