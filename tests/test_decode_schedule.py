@@ -35,7 +35,7 @@ def _segments(b0, b1, KB):
     return out
 
 
-def _run_cta(b0, b1, KB, NS, half_subtiles, multi, seed):
+def _run_cta(b0, b1, KB, NS, half_subtiles, multi, seed, fault=None):
     segs = _segments(b0, b1, KB)
     seg_stages = [-(-(e - s) // STAGE_SLABS) for (_, s, e) in segs]
     total = sum(seg_stages)
@@ -57,7 +57,8 @@ def _run_cta(b0, b1, KB, NS, half_subtiles, multi, seed):
         yield
         while pq < total:
             s = pq % NS
-            yield from wait(empty[s], ((pq // NS) & 1) ^ 1, pq // NS - 1)
+            if fault != "producer skips its wait":
+                yield from wait(empty[s], ((pq // NS) & 1) ^ 1, pq // NS - 1)
             assert empty[s].completed >= pq // NS, "ring slot refilled before its consumers read it"
             full[s].arrive()
             pq += 1
@@ -68,7 +69,7 @@ def _run_cta(b0, b1, KB, NS, half_subtiles, multi, seed):
         q = 0
         for si, stages in enumerate(seg_stages):
             buf = si & 1
-            if multi and si >= 2:
+            if multi and si >= 2 and fault != "consumer skips the segment-buffer wait":
                 yield from wait(seg_free[buf], ((si - 2) >> 1) & 1, (si - 2) >> 1)
                 assert seg_free[buf].completed >= ((si - 2) >> 1) + 1, "segment buffer reused before release"
             if w == 0:
@@ -79,7 +80,9 @@ def _run_cta(b0, b1, KB, NS, half_subtiles, multi, seed):
             for i in range(start, stages, step):
                 qs = q + i
                 s = qs % NS
-                yield from wait(full[s], (qs // NS) & 1, qs // NS)
+                parity = (qs // NS) & 1
+                yield from wait(full[s], parity ^ 1 if fault == "consumer waits on the wrong parity" else parity,
+                                qs // NS)
                 assert full[s].completed >= qs // NS + 1
                 consumed[w].append(qs)
                 empty[s].arrive()
@@ -97,8 +100,9 @@ def _run_cta(b0, b1, KB, NS, half_subtiles, multi, seed):
     def combine():
         for si in range(len(seg_stages) - 1):
             buf = si & 1
-            yield from wait(seg_full[buf], (si >> 1) & 1, si >> 1)
-            assert buffer_owner[buf] == si
+            if fault != "combine skips its wait":
+                yield from wait(seg_full[buf], (si >> 1) & 1, si >> 1)
+            assert buffer_owner[buf] == si, "segment buffer released before its consumers filled it"
             buffer_owner[buf] = None
             seg_free[buf].arrive()
             yield
@@ -131,6 +135,25 @@ def test_decode_protocol_has_no_aliasing_and_no_deadlock(M, K, N, blocks):
     for i in picks:
         for seed in range(3):
             _run_cta(bounds[i], bounds[i + 1], KB, NS, half_subtiles, multi, seed=100 * i + seed)
+
+
+FAULTS = ["producer skips its wait", "consumer skips the segment-buffer wait", "consumer waits on the wrong parity",
+          "combine skips its wait"]
+
+
+@pytest.mark.parametrize("fault", FAULTS)
+@pytest.mark.parametrize("half_subtiles", [False, True])
+def test_planted_protocol_fault_is_caught(fault, half_subtiles):
+    # The replay's checks are tight enough: each fault, planted in the model, trips one of them on
+    # some interleaving of runs with several segments.
+    caught = 0
+    for (b0, b1, KB) in [(0, 300, 128), (100, 140, 7), (0, 129, 64)]:
+        for seed in range(6):
+            try:
+                _run_cta(b0, b1, KB, 8, half_subtiles, multi=True, seed=seed, fault=fault)
+            except AssertionError:
+                caught += 1
+    assert caught > 0, f"not caught: {fault}"
 
 
 @pytest.mark.parametrize("NS", [6, 8, 10])

@@ -80,7 +80,7 @@ class Walk:
             self.ns = min(STAGE_UNITS, self.seg_end - self.u)
 
 
-def _run_cta(b0, b1, KB, n_mma, seed):
+def _run_cta(b0, b1, KB, n_mma, seed, fault=None):
     rng = random.Random(seed)
     NW, NB, NA, kI = (10, 4, 4, 2) if n_mma == 64 else (8, 3, 3, 1)
     C = 4   # converter warps modelled (the kernel's 16 arrive the same way, one arrival per warp)
@@ -100,7 +100,7 @@ def _run_cta(b0, b1, KB, n_mma, seed):
         it, q = Walk(b0, b1, KB), 0
         while not it.done():
             s = q % NW
-            if q >= NW:
+            if q >= NW and fault != "weight producer skips its wait":
                 yield from wait(wempty[s], ((q // NW) & 1) ^ 1, q // NW - 1)
             # overwriting slot s: every converter warp has read stage q - NW
             assert q < NW or wempty[s].completed >= q // NW, "weight slot overwritten before it was read"
@@ -113,7 +113,7 @@ def _run_cta(b0, b1, KB, n_mma, seed):
         it, q = Walk(b0, b1, KB), 0
         while not it.done():
             s = q % NB
-            if q >= NB:
+            if q >= NB and fault != "activation producer skips its wait":
                 yield from wait(bdone[s], ((q - NB) // NB) & 1, (q - NB) // NB)
             assert q < NB or bdone[s].completed >= (q - NB) // NB + 1, "activation slot overwritten under the MMAs"
             bfull[s].arrive()
@@ -125,9 +125,10 @@ def _run_cta(b0, b1, KB, n_mma, seed):
         it = Walk(b0, b1, KB)
         while not it.done():
             sb, a, db = it.q % NB, it.q % NA, it.period & 1
-            if it.period_first() and it.period >= 2:
+            if it.period_first() and it.period >= 2 and fault != "issuer skips the read-out wait":
                 yield from wait(dempty[db], ((it.period >> 1) - 1) & 1, (it.period >> 1) - 1)
-            yield from wait(conv[a], (it.q // NA) & 1, it.q // NA)
+            parity = (it.q // NA) & 1
+            yield from wait(conv[a], parity ^ 1 if fault == "issuer waits on the wrong parity" else parity, it.q // NA)
             # the MMAs read A slot a and activation slot sb of this stage, and write buffer db
             assert conv[a].completed >= it.q // NA + 1 and bfull[sb].completed >= it.q // NB + 1
             assert it.period < 2 or not it.period_first() or dempty[db].completed >= it.period >> 1, \
@@ -175,7 +176,8 @@ def _run_cta(b0, b1, KB, n_mma, seed):
             yield from wait(wfull[s], (it.q // NW) & 1, it.q // NW)
             if it.q >= NA:
                 qo = it.q - NA
-                yield from wait(adone[a], (qo // NA) & 1, qo // NA)
+                if fault != "converter skips the MMA wait":
+                    yield from wait(adone[a], (qo // NA) & 1, qo // NA)
                 yield from retire()
             # writing A slot a: the MMAs of stage q - NA, which read it, have completed
             assert it.q < NA or adone[a].completed >= (it.q - NA) // NA + 1, "A slot overwritten under the MMAs"
@@ -229,6 +231,27 @@ def test_protocol_has_no_aliasing_and_no_deadlock(M, K, N, blocks):
     for i in picks:
         for seed in range(3):
             _run_cta(bounds[i], bounds[i + 1], KB, n_mma, seed=1000 * i + seed)
+
+
+FAULTS = ["weight producer skips its wait", "activation producer skips its wait", "issuer skips the read-out wait",
+          "issuer waits on the wrong parity", "converter skips the MMA wait"]
+
+
+@pytest.mark.parametrize("fault", FAULTS)
+@pytest.mark.parametrize("n_mma", [64, 128])
+def test_planted_protocol_fault_is_caught(fault, n_mma):
+    # The replay's checks are tight enough: each fault, planted in the model, trips one of them on
+    # some interleaving.  Runs: long tiles (periods of four stages), and tiles of one stage each
+    # (K = 96), where a period is one stage and only the read-out wait keeps the issuer off an
+    # accumulator buffer still being read (with four-stage periods the A-ring wait implies it).
+    caught = 0
+    for (b0, b1, KB) in [(0, 300, 128), (0, 60, 3), (1, 40, 3)]:
+        for seed in range(6):
+            try:
+                _run_cta(b0, b1, KB, n_mma, seed=seed, fault=fault)
+            except AssertionError:
+                caught += 1
+    assert caught > 0, f"not caught: {fault}"
 
 
 @pytest.mark.parametrize("n_mma", [64, 128])
