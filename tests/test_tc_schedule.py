@@ -14,8 +14,8 @@ CTA runs the library's own split plans produce, and checks that
   * every role finishes (no deadlock), and
   * every stage is converted, multiplied and retired once, every period's accumulator read once.
 
-Roles (one CTA): the weight producer, the activation producer, C converter warps (each arrives
-once per warp), I issuing threads, and an MMA engine that completes each issuer's commits in
+Roles (one CTA): the weight producer, the activation producer, sixteen converter warps as in the
+kernel (each arrives once per warp), I issuing threads, and an MMA engine that completes each issuer's commits in
 order.  Ring depths are the kernel's (weight 8 / activations 3 / tensor-memory A 3 at N = 128,
 10 / 4 / 4 with two issuers at N = 64).
 """
@@ -83,7 +83,7 @@ class Walk:
 def _run_cta(b0, b1, KB, n_mma, seed, fault=None):
     rng = random.Random(seed)
     NW, NB, NA, kI = (10, 4, 4, 2) if n_mma == 64 else (8, 3, 3, 1)
-    C = 4   # converter warps modelled (the kernel's 16 arrive the same way, one arrival per warp)
+    C = 16  # converter warps, as many as the kernel runs (one arrival per warp)
     wfull = [Barrier(f"wfull{s}", 1) for s in range(NW)]
     wempty = [Barrier(f"wempty{s}", C) for s in range(NW)]
     bfull = [Barrier(f"bfull{s}", 1) for s in range(NB)]
