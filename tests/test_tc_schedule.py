@@ -15,8 +15,8 @@ CTA runs the library's own split plans produce, and checks that
   * every stage is converted, multiplied and retired once, every period's accumulator read once.
 
 Roles (one CTA): the weight producer, the activation producer, sixteen converter warps as in the
-kernel (each arrives once per warp), I issuing threads, and an MMA engine that completes each issuer's commits in
-order.  Ring depths are the kernel's (weight 8 / activations 3 / tensor-memory A 3 at N = 128,
+kernel (each arrives once per warp), I issuing threads, and an MMA engine that completes each
+issuer's commits in order.  Ring depths are the kernel's (weight 8 / activations 3 / tensor-memory A 3 at N = 128,
 10 / 4 / 4 with two issuers at N = 64).
 """
 import random
