@@ -46,3 +46,16 @@ def test_reference_arm_prints_one_contract_line():
     assert out["e2e"] == {"value": out["value"], "unit": out["unit"], "h2d_bytes_per_step": 0,
                           "d2h_bytes_per_step": 0}
     assert out["config"]["workload"]
+
+
+def test_device_arm_fails_loudly_without_a_gpu():
+    # No CPU fallback: on a host without CUDA the default (device) arm exits non-zero and prints no
+    # result line.
+    import torch
+    if torch.cuda.is_available():
+        import pytest
+        pytest.skip("a GPU is present")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "1", "--warmup", "3"], cwd=ROOT,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0
+    assert not [ln for ln in r.stdout.splitlines() if ln.strip().startswith("{")]
