@@ -7,6 +7,9 @@ import statistics
 import subprocess
 import sys
 
+import pytest
+import torch
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
 
@@ -51,9 +54,7 @@ def test_reference_arm_prints_one_contract_line():
 def test_device_arm_fails_loudly_without_a_gpu():
     # No CPU fallback: on a host without CUDA the default (device) arm exits non-zero and prints no
     # result line.
-    import torch
     if torch.cuda.is_available():
-        import pytest
         pytest.skip("a GPU is present")
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "1", "--warmup", "3"], cwd=ROOT,
                        capture_output=True, text=True, timeout=300)
