@@ -707,7 +707,7 @@ def run_ncu_driver(args):
         sys.exit(1)
 
 
-def main():
+def build_parser():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
@@ -722,6 +722,11 @@ def main():
     ap.add_argument("--ncu-shape", default="", help="M,K,N for --ncu-driver (default: the headline shape)")
     ap.add_argument("--ncu-driver", type=int, default=0,
                     help="profiling driver: this many eager calls of the default workload, then exit")
+    return ap
+
+
+def main():
+    ap = build_parser()
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -60,3 +60,20 @@ def test_device_arm_fails_loudly_without_a_gpu():
                        capture_output=True, text=True, timeout=300)
     assert r.returncode != 0
     assert not [ln for ln in r.stdout.splitlines() if ln.strip().startswith("{")]
+
+
+def test_profile_summaries_quote_commands_the_bench_accepts():
+    # Every bench command a committed ncu summary gives must still parse with the current options,
+    # so that the summary can be reproduced from committed files.
+    import re
+    import shlex
+
+    prof = os.path.join(ROOT, "profiles")
+    found = 0
+    for name in sorted(os.listdir(prof)):
+        with open(os.path.join(prof, name)) as f:
+            text = f.read()
+        for cmd in re.findall(r"python bench\.py([^`|&>\n\\]*)", text):
+            bench.build_parser().parse_args(shlex.split(cmd))
+            found += 1
+    assert found > 0
