@@ -11,6 +11,7 @@ import itertools
 import os
 import subprocess
 
+import numpy as np
 import pytest
 
 import oracle
@@ -128,4 +129,38 @@ def test_control_build_passes_every_pin(source, tmp_path, monkeypatch):
 def test_planted_mistake_fails_a_pin(name, old, new, filters, source, tmp_path, monkeypatch):
     assert source.count(old) == 1, f"snippet for '{name}' must occur exactly once"
     _use(monkeypatch, _build(source.replace(old, new), str(tmp_path), "mutant"))
+    assert _first_failing_pin(filters) is not None, f"no pin catches: {name}"
+
+
+def _bound_without_weight_norm(x_bits, q, d_bits, rel=2e-3):
+    xn, wn = oracle.q8_0_norms(x_bits, q, d_bits)
+    return rel * xn[:, None] * np.ones_like(wn)[None, :]
+
+
+def _bound_rows_reversed(x_bits, q, d_bits, rel=2e-3):
+    xn, wn = oracle.q8_0_norms(x_bits, q, d_bits)
+    return rel * np.outer(xn[::-1], wn)
+
+
+def _rms_bound_without_rs(x_bits, g_bits, eps, q, d_bits, rel=4e-3):
+    T, K = x_bits.shape
+    xg = np.zeros(T, dtype=np.float64)
+    oracle.lib().oracle_q8_0_rms_xg_norms(oracle._ptr(np.ascontiguousarray(x_bits, np.uint16)),
+                                          oracle._ptr(np.ascontiguousarray(g_bits, np.uint16)), T, K,
+                                          oracle._ptr(xg))
+    _, wn = oracle.q8_0_norms(x_bits, q, d_bits)
+    return rel * xg[:, None] * wn[None, :]
+
+
+# Mistakes in the oracle's Python-level tolerance functions: (name, attribute, replacement, filters)
+PY_MUTANTS = [
+    ("bound without the weight norm", "q8_0_bound", _bound_without_weight_norm, ["bound"]),
+    ("bound pairs the wrong activation row", "q8_0_bound", _bound_rows_reversed, ["bound"]),
+    ("rms bound without rs", "q8_0_rms_bound", _rms_bound_without_rs, ["bound"]),
+]
+
+
+@pytest.mark.parametrize("name,attr,fn,filters", PY_MUTANTS, ids=[m[0] for m in PY_MUTANTS])
+def test_planted_tolerance_mistake_fails_a_pin(name, attr, fn, filters, monkeypatch):
+    monkeypatch.setattr(oracle, attr, fn)
     assert _first_failing_pin(filters) is not None, f"no pin catches: {name}"

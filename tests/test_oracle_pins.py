@@ -289,6 +289,24 @@ def test_q8_0_norms():
     np.testing.assert_allclose(wn, np.sqrt((w * w).sum(axis=1)), rtol=1e-14)
 
 
+def test_q8_0_bound_is_the_cauchy_schwarz_scale():
+    # The per-output bound is rel * ||x_t|| * ||w_n||: by Cauchy-Schwarz |y[t,n]| never exceeds
+    # ||x_t|| ||w_n||, with equality when x_t is w_n.  Unit scales and small quants make w exact in
+    # bf16, so rows of x can be set to rows of w: the equality pins the (t, n) orientation.
+    T, K, N = 2, 64, 3
+    q = synth.uniform_int8(12, "pin.cs.q", (N, K), lo=-20, hi=20)
+    d = np.full((N, K // 32), 1.0, np.float16)
+    x = torch.tensor(np.stack([q[2], q[0]]).astype(np.float32)).to(torch.bfloat16)
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    b = oracle.q8_0_bound(xb, q, d.view(np.uint16), 2e-3)
+    y = oracle.q8_0_gemv(xb, q, d.view(np.uint16))
+    assert b.shape == (T, N)
+    assert (np.abs(y) <= b / 2e-3 * (1 + 1e-12)).all()
+    for t, n in ((0, 2), (1, 0)):
+        assert y[t, n] == pytest.approx(b[t, n] / 2e-3, rel=1e-12)
+        assert y[t, n] == float((q[n].astype(np.int64) ** 2).sum())
+
+
 def test_q8_0_split_layout_from_ggml_blocks():
     # The split layout is the same bytes as ggml's 34-byte blocks, reordered.
     K, N = 64, 3
