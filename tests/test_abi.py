@@ -376,3 +376,18 @@ def test_emulated_fragment_path_reproduces_x_at_w():
                                 acc[n, :] += a * xp[:, slot_k[slot]]
     ref = oracle.w8a8_acc(x, W)
     np.testing.assert_array_equal(acc[:N, :M].T, ref)
+
+
+def test_workspace_query_covers_every_smaller_m_across_shapes():
+    # The size query's promise: a workspace of w8a8_workspace_bytes(M_max, K, N, blocks) bytes
+    # serves every call with M <= M_max, whichever arm and kernel variant that M runs.
+    rng = np.random.default_rng(17)
+    shapes = [(32, 8), (96, 136), (512, 256), (4096, 1536), (4096, 2560), (12288, 4096), (4096, 24576)]
+    for K, N in shapes:
+        for M_max in (1, 8, 17, 32, 33, 64, 65, 100, 128):
+            for blocks in (0, 1, int(rng.integers(2, 64))):
+                big = lib8.w8a8_workspace_bytes(M_max, K, N, blocks)
+                if big == 0:      # some M <= M_max has no plan with this many CTAs
+                    continue
+                for M in range(1, M_max + 1):
+                    assert lib8.w8a8_plan(M, K, N, blocks)["workspace_bytes"] <= big, (M, M_max, K, N, blocks)
