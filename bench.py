@@ -1,16 +1,18 @@
 #!/usr/bin/env python3
 """Benchmark: weight-stream GB/s and us/call of the int8 decode GEMM (M <= 32), cold-L2 graph replay.
 
-Workload (default): W8A8 GEMM M=16, K=4096, N=1536 (a fused-QKV-like decode shape), int8 x_q and W
-uniform in [-127, 127], fp32 scales uniform in [1e-3, 2e-2], seeded synthetic data.  R rotating
-packed-W buffers, R = max(16, ceil(3 * L2 / W_bytes)), so every call streams its weight cold from
-HBM (inputs larger than L2; no flush needed).  One step = one CUDA-graph replay of C calls cycling
+Workload (default): W8A8 GEMM M=16, K=4096, N=24576, the MLP gate_up decode shape (the largest
+single-GPU decode shape of the workloads), int8 x_q and W from a clipped Gaussian (sigma 40, clip
++-127), fp32 scales log-uniform in [1e-4, 1e-1], seeded synthetic data.  R rotating packed-W
+buffers, R = max(16, ceil(3 * L2 / W_bytes)), so every call streams its weight cold from HBM
+(inputs larger than L2; no flush needed).  One step = one CUDA-graph replay of C calls cycling
 through the R buffers.  W warm-up steps, then K timed steps bracketed by a barrier and a device
 synchronise, timed with CUDA events on the launching stream; max over ranks.
 
-Beside the headline the line reports the same call launched with PDL, an end-to-end leg with host
-buffers, the Q8_0 reads (plain and RMS-norm), the quantisation rows, the 32 < M <= 128 arm at
-M = 128 (tensor_memory_arm), the read ceiling and the oracle's CPU baseline.
+Beside the headline the line reports the same call launched with PDL, the MLP down shape and the
+fused-QKV-like shape (plain and PDL), an end-to-end leg with host buffers, the Q8_0 reads (plain
+and RMS-norm), the quantisation rows, the 32 < M <= 128 arm at M = 128 (tensor_memory_arm), the
+read ceiling and the oracle's CPU baseline (one thread and all host cores).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--sweep]
 Under torchrun each rank runs an independent replica (the operator has no exchange step).
@@ -34,9 +36,32 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "weight-stream GB/s and us/call, int8 decode GEMM M<=32, cold-L2 graph replay"
-DEFAULT = dict(M=16, K=4096, N=1536, dist="uniform", seed=1)
-KERNEL_SOURCES = ["int8_weight_gemm_gb300/csrc/w8a8_gemm.cu", "int8_weight_gemm_gb300/csrc/common.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "w8a8_gemm_m16_k4096_n1536_traffic.txt")
+DATA = {"mlp": "synthetic (seeded SplitMix64 streams; int8 clipped Gaussian sigma=40 clip +-127, fp32 scales "
+               "log-uniform [1e-4,1e-1])",
+        "uniform": "synthetic (seeded SplitMix64 streams; int8 U[-127,127], fp32 scales U[1e-3,2e-2])"}
+# The decode shapes the line reports: the headline (timed as `value`) and the shapes beside it.
+WORKLOADS = {
+    "gate_up": dict(M=16, K=4096, N=24576, dist="mlp", seed=4, label="MLP gate_up decode shape"),
+    "down": dict(M=16, K=12288, N=4096, dist="mlp", seed=4, label="MLP down decode shape"),
+    "qkv": dict(M=16, K=4096, N=1536, dist="uniform", seed=1, label="fused-QKV-like decode shape"),
+}
+HEADLINE = "gate_up"
+DEFAULT = WORKLOADS[HEADLINE]
+# Sources of the timed kernel and its plan: the committed DRAM-traffic figure is valid only while
+# these are unchanged.
+KERNEL_SOURCES = ["int8_weight_gemm_gb300/csrc/w8a8_gemm.cu", "int8_weight_gemm_gb300/csrc/common.cuh",
+                  "int8_weight_gemm_gb300/csrc/internal.h", "int8_weight_gemm_gb300/csrc/api.cu"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "w8a8_gemm_m16_k4096_n24576_traffic.txt")
+
+
+def workload_config(name: str, world: int) -> dict:
+    """The `config` object of a bench line for one workload (shared by both arms)."""
+    w = WORKLOADS[name]
+    return {"workload": f"W8A8 GEMM M={w['M']}, K={w['K']}, N={w['N']} ({w['label']})",
+            "M": w["M"], "K": w["K"], "N": w["N"], "dist": w["dist"], "seed": w["seed"],
+            "l2": "inputs larger than L2: each call streams a different packed W buffer, rotating over "
+                  "max(16, ceil(3 x L2 / W bytes)) buffers",
+            "parallelism": f"replicas x{world}"}
 
 
 def rank_barrier():
@@ -176,10 +201,47 @@ class ClockSampler:
 # CPU baseline: the oracle as it stands, on the host cores, on a bounded sample of the workload
 # ---------------------------------------------------------------------------------------------
 
-def cpu_baseline(M, K, N, x, xs, W, ws, budget_s=12.0, cols=None):
+def host_cores() -> int:
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+class OracleOnCores:
+    """The oracle's W8A8 GEMM (plain C, one thread per call) over all host cores: the columns of W
+    are cut into one contiguous slice per thread and each thread calls the oracle on its slice
+    (ctypes releases the interpreter lock for the call).  Columns are independent, so the slices
+    together give the whole result; the oracle itself is used as it stands."""
+
+    def __init__(self, x, xs, W, ws, threads=None, cols=None):
+        import concurrent.futures as cf
+
+        N = W.shape[1] if cols is None else cols
+        self.threads = max(1, min(threads or host_cores(), N // 8))
+        cuts = [round(i * N / self.threads) for i in range(self.threads + 1)]
+        self.parts = [(np.ascontiguousarray(W[:, a:b]), np.ascontiguousarray(ws[a:b]))
+                      for a, b in zip(cuts[:-1], cuts[1:])]
+        self.x, self.xs, self.N = x, xs, N
+        self.pool = cf.ThreadPoolExecutor(max_workers=self.threads)
+
+    def call(self):
+        import oracle
+
+        futs = [self.pool.submit(oracle.w8a8_gemm, self.x, self.xs, Wp, wp) for Wp, wp in self.parts]
+        return np.concatenate([f.result() for f in futs], axis=1)
+
+    def close(self):
+        self.pool.shutdown()
+
+
+def cpu_baseline(M, K, N, x, xs, W, ws, budget_s=8.0):
+    """The oracle timed on the host: one thread on a column sample, then all host cores on the
+    whole workload (threads over column slices), each for about budget_s seconds."""
     import oracle
 
-    cols = cols or N
+    cols = min(N, 2048)
     Ws = np.ascontiguousarray(W[:, :cols])
     wss = np.ascontiguousarray(ws[:cols])
     calls = 0
@@ -190,11 +252,25 @@ def cpu_baseline(M, K, N, x, xs, W, ws, budget_s=12.0, cols=None):
         el = time.perf_counter() - t0
         if el >= budget_s or calls >= 200:
             break
+    single = {"value": K * cols / (el / calls) / 1e9, "unit": "GB/s", "cores": 1,
+              "sample": f"{calls} oracle calls on M={M}, K={K}, N={cols} (of {N}) columns, one thread, "
+                        f"{el / calls * 1e3:.1f} ms/call"}
+    par = OracleOnCores(x, xs, W, ws)
+    par.call()
+    calls = 0
+    t0 = time.perf_counter()
+    while True:
+        par.call()
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or calls >= 200:
+            break
+    par.close()
     per_call = el / calls
-    gbs = K * cols / per_call / 1e9
-    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{calls} oracle calls on M={M}, K={K}, N={cols} (of {N}) columns, single thread, "
-                      f"{per_call * 1e3:.1f} ms/call"}
+    return {"value": K * N / per_call / 1e9, "unit": "GB/s", "cores": par.threads, "kind": "oracle",
+            "sample": f"{calls} whole calls of M={M}, K={K}, N={N}, the columns cut over {par.threads} threads "
+                      f"(one per host core), {per_call * 1e3:.1f} ms/call",
+            "single_thread": single}
 
 
 # ---------------------------------------------------------------------------------------------
@@ -499,6 +575,23 @@ def time_q8(T, K, N, iters=200, seed=7, flags=0, rms=False):
             "GBps": nbytes / statistics.median(samples) / 1e3}
 
 
+def shape_summary(name, res, peak, world):
+    """One beside-the-headline entry: median / p90 us per call, GB/s and roofline fraction."""
+    w = WORKLOADS[name]
+    alg = alg_bytes(w["M"], w["K"], w["N"])
+    return {"workload": workload_config(name, world)["workload"], "kernel": res["kernel"], "blocks": res["blocks"],
+            "us_per_call": {"median": round(res["us_median"], 4), "p90": round(res["us_p90"], 4)},
+            "weight_GBps": round(res["wbytes"] / (res["us_median"] * 1e-6) / 1e9, 1),
+            "roofline_frac": round(alg / (res["avg_launch_us"] * 1e-6) / 1e9 / peak, 4),
+            "rotating_weight_buffers": res["R"]}
+
+
+def alg_bytes(M, K, N):
+    """Algorithmic bytes of one W8A8 call: the weight, the activations and both scale vectors read,
+    the bf16 output written."""
+    return K * N + M * K + 4 * M + 4 * N + 2 * M * N
+
+
 def run_ours(args):
     import torch
 
@@ -510,15 +603,14 @@ def run_ours(args):
         torch.distributed.init_process_group("nccl")
     dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
     cfg = DEFAULT
-    res = time_gemm(cfg["M"], cfg["K"], cfg["N"], cfg["dist"], cfg["seed"], args.steps, args.warmup,
-                    device=dev, sample_clocks=(rank == 0))
     M, K, N = cfg["M"], cfg["K"], cfg["N"]
+    res = time_gemm(M, K, N, cfg["dist"], cfg["seed"], args.steps, args.warmup, device=dev, sample_clocks=(rank == 0))
     x, xs, W, ws = res.pop("inputs")
     wbytes = res["wbytes"]
     value = whole_job_gbs(world, wbytes, res["launches"], res["total_ms"])
     peak, peak_kind = _peaks()
-    alg_bytes = K * N + M * K + 4 * M + 4 * N + 2 * M * N
-    achieved = alg_bytes / (res["avg_launch_us"] * 1e-6) / 1e9
+    alg = alg_bytes(M, K, N)
+    achieved = alg / (res["avg_launch_us"] * 1e-6) / 1e9
     traffic = _traffic_per_launch()
     out = {
         "metric": METRIC,
@@ -532,17 +624,15 @@ def run_ours(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "int8",
-        "data": "synthetic (seeded SplitMix64 streams; int8 U[-127,127], fp32 scales U[1e-3,2e-2])",
-        "config": {"workload": f"W8A8 GEMM M={M}, K={K}, N={N} (fused-QKV-like decode shape)",
-                   "M": M, "K": K, "N": N, "rotating_weight_buffers": res["R"], "calls_per_step": res["C"],
-                   "l2": "inputs larger than L2: each call streams a different packed W buffer "
-                         f"({res['R']} x {wbytes / 2**20:.1f} MiB rotating)",
-                   "parallelism": f"replicas x{world}"},
+        "data": DATA[cfg["dist"]],
+        "config": workload_config(HEADLINE, world),
+        "timing": {"rotating_weight_buffers": res["R"], "calls_per_step": res["C"],
+                   "weight_bytes_per_call": wbytes, "steps": args.steps},
         "us_per_call": {"median": round(res["us_median"], 4), "p90": round(res["us_p90"], 4)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} (copy, MEASURED_PEAKS.json hbm_gbs)",
-                     "traffic": traffic, "alg_bytes_per_launch": alg_bytes,
-                     "kernel": res["kernel"]},
+                     "traffic": traffic, "alg_bytes_per_launch": alg,
+                     "frac_of_8tbs_nominal": round(achieved / 8000.0, 4), "kernel": res["kernel"]},
         "gpu_launches": res["launches"],
         "e2e": {k: (round(v, 3) if isinstance(v, float) else v) for k, v in res["e2e"].items()},
         "clocks": res["clocks"],
@@ -556,16 +646,35 @@ def run_ours(args):
     rp.pop("inputs")
     out["pdl"] = {"value": round(whole_job_gbs(world, wbytes, rp["launches"], rp["total_ms"]), 2), "unit": "GB/s",
                   "us_per_call": {"median": round(rp["us_median"], 4), "p90": round(rp["us_p90"], 4)},
-                  "roofline_frac": round(alg_bytes / (rp["avg_launch_us"] * 1e-6) / 1e9 / peak, 4),
+                  "roofline_frac": round(alg / (rp["avg_launch_us"] * 1e-6) / 1e9 / peak, 4),
                   "launch": "W8A8_FLAG_PDL, same graph of rotating-weight calls"}
     del rp
-    # one-call correctness check of the timed configuration against the oracle (first 4 rows)
+    # The other decode shapes, plain and with PDL.
+    out["shapes"] = []
+    for name in ("down", "qkv"):
+        w = WORKLOADS[name]
+        entry = None
+        for flags in (0, lib8.W8A8_FLAG_PDL):
+            r = time_gemm(w["M"], w["K"], w["N"], w["dist"], w["seed"], min(args.steps, 300), args.warmup, device=dev,
+                          want_e2e=False, flags=flags)
+            r.pop("inputs")
+            if flags == 0:
+                entry = shape_summary(name, r, peak, world)
+            else:
+                entry["pdl_us_per_call"] = {"median": round(r["us_median"], 4), "p90": round(r["us_p90"], 4)}
+            del r
+            torch.cuda.empty_cache()
+        out["shapes"].append(entry)
+    # Correctness check of the timed configuration against the oracle: every row, a seeded sample of
+    # whole columns (the first and last of every 64-row tile among them).
     if rank == 0:
         import oracle
-        ref = oracle.w8a8_gemm(x[:4], xs[:4], W, ws)
-        got = res["out"][:4].cpu().view(torch.int16).numpy().view(np.uint16)
-        out["parity_rows_checked"] = int(4)
-        out["parity_mismatches"] = int(np.count_nonzero(got != ref))
+        rng = np.random.default_rng(12345)
+        cols = np.unique(np.concatenate([rng.choice(N, 256, replace=False), np.arange(0, N, 64), np.arange(63, N, 64)]))
+        ref = oracle.w8a8_gemm(x, xs, np.ascontiguousarray(W[:, cols]), np.ascontiguousarray(ws[cols]))
+        got = res["out"].cpu().view(torch.int16).numpy().view(np.uint16)[:, cols]
+        out["parity"] = {"outputs_checked": int(ref.size), "columns_checked": int(len(cols)),
+                         "mismatches": int(np.count_nonzero(got != ref))}
         if not args.no_q8:
             out["q8_0"] = [time_q8(T, K8, N8, flags=f) for (K8, N8) in ((4096, 320), (320, 4096)) for T in (1, 4, 6)
                            for f in (0, lib8.W8A8_FLAG_PDL)]
@@ -587,32 +696,32 @@ def run_ours(args):
 
 
 def run_reference(args):
-    """The oracle timed on the host cores on the same metric, config and unit (a bounded sample per step)."""
+    """The oracle timed on the host cores on the same metric, config and unit: every step is one
+    whole call of the headline workload, its columns cut over one thread per host core.  Under
+    torchrun only rank 0 runs it."""
     rank = _env_int("RANK", 0)
     if rank != 0:
         return
-    import oracle
     import synth
 
     cfg = DEFAULT
     M, K, N = cfg["M"], cfg["K"], cfg["N"]
     x, xs, W, ws = synth.w8a8_inputs(M, K, N, seed=cfg["seed"], dist=cfg["dist"])
-    cols = 128
-    Ws = np.ascontiguousarray(W[:, :cols])
-    wss = np.ascontiguousarray(ws[:cols])
+    par = OracleOnCores(x, xs, W, ws)
     for _ in range(args.warmup):
-        oracle.w8a8_gemm(x, xs, Ws, wss)
+        par.call()
     times = []
     t0 = time.perf_counter()
     for _ in range(args.steps):
         a = time.perf_counter()
-        oracle.w8a8_gemm(x, xs, Ws, wss)
+        par.call()
         times.append(time.perf_counter() - a)
     total = time.perf_counter() - t0
-    value = K * cols * args.steps / total / 1e9
+    par.close()
+    value = K * N * args.steps / total / 1e9
     times.sort()
-    sample = (f"each step: one oracle call on M={M}, K={K}, N={cols} columns (a slice of N={N}), "
-              "single thread, plain C")
+    sample = (f"each step: one whole oracle call of M={M}, K={K}, N={N}, its columns cut over {par.threads} "
+              "threads (one per host core), plain C")
     out = {
         "impl": "reference",
         "metric": METRIC,
@@ -626,12 +735,11 @@ def run_reference(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "int64",
-        "data": "synthetic (seeded SplitMix64 streams; int8 U[-127,127], fp32 scales U[1e-3,2e-2])",
-        "config": {"workload": f"W8A8 GEMM M={M}, K={K}, N={N} (fused-QKV-like decode shape)", "M": M, "K": K,
-                   "N": N, "sample_columns": cols},
-        "us_per_call": {"median": round(statistics.median(times) * 1e6, 1),
-                        "p90": round(p90(times) * 1e6, 1)},
-        "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": sample, "value": round(value, 4), "unit": "GB/s"},
+        "data": DATA[cfg["dist"]],
+        "config": workload_config(HEADLINE, _env_int("WORLD_SIZE", 1)),
+        "us_per_call": {"median": round(statistics.median(times) * 1e6, 1), "p90": round(p90(times) * 1e6, 1)},
+        "cpu_baseline": {"kind": "oracle", "cores": par.threads, "sample": sample, "value": round(value, 4),
+                         "unit": "GB/s"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }

@@ -72,7 +72,16 @@ enum {
      * are not written by work still in flight on the stream (weights are load-time constants: pack
      * them, then synchronise once).  Consecutive calls then overlap one call's weight prefetch with
      * the previous call's tail, inside a CUDA graph as well. */
-    W8A8_FLAG_PDL = 1u
+    W8A8_FLAG_PDL = 1u,
+    /* Test hook of the device fault path (w8a8_gemm and its variants only; not for production
+     * calls).  One warp of the first CTA waits on a pipeline barrier that nothing completes, with a
+     * bound of a few milliseconds instead of the usual second.  The wait runs out, the kernel
+     * records W8A8_DEV_WAIT_TIMEOUT in the workspace status word, and every CTA returns: the rest
+     * of that CTA gives up at its next wait, after the copies it issued have landed and the tensor
+     * memory it holds is freed.  The host call itself returns W8A8_OK; the output is undefined and
+     * the workspace must be zeroed again (w8a8_workspace_init) before its next use.  No GPU fault
+     * and no hang is involved: it exercises the same bounded-wait exit that a real timeout takes. */
+    W8A8_FLAG_TEST_STALL = 0x100u
 };
 
 /* Library version (major * 10000 + minor * 100 + patch). */
@@ -151,7 +160,8 @@ int w8a8_pack_weights(const int8_t* W, int K, int N, void* W_packed, void* ws, s
  *           the SM count, at most one CTA per slab).  Must not exceed the number of slabs.
  *           For M > 32 the same rule applies to T = ceil(N/128) tiles of 128 rows (two packed
  *           tiles each) x KB units of 32 k, with one CTA per SM by default.
- *  flags    0 or W8A8_FLAG_PDL; any other bit is INVALID_ARG.
+ *  flags    0 or W8A8_FLAG_PDL (W8A8_FLAG_TEST_STALL for tests of the fault path); any other bit
+ *           is INVALID_ARG.
  *  ws       workspace of at least w8a8_workspace_bytes(M, K, N, blocks) bytes.
  *  The int32 sums are exact (the result does not depend on `blocks`), and the epilogue order is
  *  fixed, so the output is bit-identical for every `blocks` and every replay.
@@ -159,6 +169,18 @@ int w8a8_pack_weights(const int8_t* W, int K, int N, void* W_packed, void* ws, s
 int w8a8_gemm(const int8_t* x_q, const float* x_scale, const void* W_packed, const float* w_scale,
               void* out, int M, int K, int N, int blocks, unsigned flags, void* ws, size_t ws_bytes,
               void* stream);
+
+/* The same call as w8a8_gemm, which in addition stores the exact int32 sums
+ *   acc[m][n] = sum_k x_q[m][k] * W[k][n]
+ * that its epilogue scales, into `acc` ([M,N] int32 row-major, 4-byte aligned, device memory;
+ * rows m >= M and columns n >= N are never written).  The W8A8 page's cross-shape rules make the
+ * int32 accumulation exact and its outputs bit-identical across splits; this entry point exposes
+ * the accumulators so that they can be checked against a reference bit for bit, not only through
+ * the bf16 rounding.  The same kernel runs, with one more store per output element.
+ * Errors: those of w8a8_gemm, and INVALID_ARG for a NULL acc, MISALIGNED for a misaligned one. */
+int w8a8_gemm_acc(const int8_t* x_q, const float* x_scale, const void* W_packed, const float* w_scale,
+                  void* out, int32_t* acc, int M, int K, int N, int blocks, unsigned flags, void* ws,
+                  size_t ws_bytes, void* stream);
 
 /* Launch plan of a w8a8_gemm call (host-only query; launches nothing). */
 typedef struct {
@@ -194,20 +216,31 @@ int w8a8_split_bounds_m(int M, int K, int N, int blocks, long long* bounds, int 
  * plugin that sees only the input and output pointers its host engine hands it, or a request path
  * that must not call cudaMalloc (which can synchronise the device and stall other streams).
  *
- * Arguments, limits, result and errors are those of w8a8_gemm, without ws / ws_bytes.  The
- * workspace is a 16 MiB area inside this library's device memory (a file-scope __device__ array,
- * held on every device that loads the library until the process exits); a shape whose
- * w8a8_workspace_bytes(M, K, N, blocks) exceeds 16 MiB returns W8A8_ERR_WORKSPACE_TOO_SMALL.
- * Each call clears the part of the area it uses (one cudaMemsetAsync on `stream`) and then
- * launches the kernel; it calls no allocating routine.
+ * Arguments, limits and result are those of w8a8_gemm, without ws / ws_bytes; flags as for
+ * w8a8_gemm.  The workspace is a 16 MiB area inside this library's device memory (a file-scope
+ * __device__ array, held on every device that loads the library until the process exits); a shape
+ * whose w8a8_workspace_bytes(M, K, N, blocks) exceeds 16 MiB returns W8A8_ERR_WORKSPACE_TOO_SMALL.
+ * Each call clears the part of the area its kernel needs zeroed (one cudaMemsetAsync on `stream`)
+ * and then launches the kernel; it calls no allocating routine.
  *
- * The first call on a device looks up the area's device address (cudaGetSymbolAddress, with that
- * device current) and caches it; make that first call before any stream capture on the device.
- * All calls on a device share the one area, so calls whose kernels can overlap on the GPU (on
- * different streams without ordering between them) race on it and give undefined results. */
+ * The first call in a CUDA context looks up the area's device address (cudaGetSymbolAddress, in
+ * that context) and caches it per context; make that first call before any stream capture.  A
+ * context created later (another context on the device, or the primary context again after
+ * cudaDeviceReset) gets its own look-up on its first call.  All calls in a context share the one
+ * area, so calls whose kernels can overlap on the GPU (on different streams without ordering
+ * between them) race on it and give undefined results.
+ *
+ * Device faults (W8A8_DEV_*) are OR-ed into the area's status word, which no call clears: read it
+ * with w8a8_gemm_no_alloc_status. */
 int w8a8_gemm_no_alloc(const int8_t* x_q, const float* x_scale, const void* W_packed,
                        const float* w_scale, void* out, int M, int K, int N, int blocks,
                        unsigned flags, void* stream);
+
+/* Read the device status word of w8a8_gemm_no_alloc's area in the current context into *status
+ * (0 = no device fault recorded since the last read; otherwise W8A8_DEV_* bits of any call since
+ * then), and clear it.  Synchronises `stream` (a host read): not for use inside a capture.  Errors:
+ * INVALID_ARG (status NULL), CUDA. */
+int w8a8_gemm_no_alloc_status(void* stream, uint32_t* status);
 
 /* -------------------------------------------------------------------------------------------
  * Q8_0 weight GEMV (verify window)

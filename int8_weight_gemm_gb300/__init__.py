@@ -26,6 +26,7 @@ __all__ = [
     "w8a8_workspace_status",
     "w8a8_pack_weights",
     "w8a8_gemm",
+    "w8a8_gemm_acc",
     "q8_0_gemv",
     "q8_0_gemv_rms",
     "w8a8_plan",
@@ -40,6 +41,7 @@ __all__ = [
 
 W8A8_OK = 0
 W8A8_FLAG_PDL = 1
+W8A8_FLAG_TEST_STALL = 0x100
 W8A8_DEV_WAIT_TIMEOUT = 1
 W8A8_DEV_COUNTER_CORRUPT = 2
 
@@ -77,7 +79,10 @@ SIGNATURES = {
     "w8a8_workspace_bytes": ([_c_i, _c_i, _c_i, _c_i], _c_sz),
     "w8a8_pack_weights": ([_c_p, _c_i, _c_i, _c_p, _c_p, _c_sz, _c_p], _c_i),
     "w8a8_gemm": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_i, _c_i, _c_i, _c_i, ctypes.c_uint, _c_p, _c_sz, _c_p], _c_i),
+    "w8a8_gemm_acc": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i, _c_i, _c_i, _c_i, ctypes.c_uint, _c_p, _c_sz, _c_p],
+                      _c_i),
     "w8a8_gemm_no_alloc": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_i, _c_i, _c_i, _c_i, ctypes.c_uint, _c_p], _c_i),
+    "w8a8_gemm_no_alloc_status": ([_c_p, ctypes.POINTER(ctypes.c_uint32)], _c_i),
     "w8a8_plan": ([_c_i, _c_i, _c_i, _c_i, ctypes.POINTER(PlanT)], _c_i),
     "w8a8_split_bounds": ([_c_i, _c_i, _c_i, ctypes.POINTER(ctypes.c_longlong), _c_i], _c_i),
     "w8a8_split_bounds_m": ([_c_i, _c_i, _c_i, _c_i, ctypes.POINTER(ctypes.c_longlong), _c_i], _c_i),
@@ -263,6 +268,30 @@ def w8a8_gemm(x_q, x_scale, W_packed, w_scale, ws, N: int, out=None, blocks: int
                          flags, _ptr(ws), _nbytes(ws), _stream(stream))
     _check("w8a8_gemm", rc)
     return out
+
+
+def w8a8_gemm_acc(x_q, x_scale, W_packed, w_scale, ws, N: int, out=None, acc=None, blocks: int = 0, flags: int = 0,
+                  stream=None):
+    """w8a8_gemm that also returns the exact int32 sums: (out [M,N] bf16, acc [M,N] int32)."""
+    import torch
+
+    M, K = x_q.shape
+    _dev(x_q, "x_q", esize=1)
+    _dev(x_scale, "x_scale", 4 * M)
+    _dev(W_packed, "W_packed", w8a8_packed_weight_bytes(K, N))
+    _dev(w_scale, "w_scale", 4 * N)
+    _dev(ws, "ws")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x_q.device)
+    if acc is None:
+        acc = torch.empty((M, N), dtype=torch.int32, device=x_q.device)
+    _dev(out, "out", 2 * M * N)
+    _dev(acc, "acc", 4 * M * N, esize=4)
+    _on_cuda(x_q=x_q, x_scale=x_scale, W_packed=W_packed, w_scale=w_scale, ws=ws, out=out, acc=acc)
+    rc = lib().w8a8_gemm_acc(_ptr(x_q), _ptr(x_scale), _ptr(W_packed), _ptr(w_scale), _ptr(out), _ptr(acc), M, K, N,
+                             blocks, flags, _ptr(ws), _nbytes(ws), _stream(stream))
+    _check("w8a8_gemm_acc", rc)
+    return out, acc
 
 
 def _q8_args(x, q, d, ws, K, N):

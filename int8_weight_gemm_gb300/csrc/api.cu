@@ -91,9 +91,9 @@ int any_plan(int M, int K, int N, int blocks, int sm_count, AnyPlan* plan) {
 }
 
 cudaError_t any_launch(const AnyPlan& pl, const int8_t* x, const float* xs, const void* wp, const float* wsc, void* out,
-                       int M, int K, int N, void* ws, bool pdl, cudaStream_t stream) {
-  return pl.tc ? tc_launch(pl.t, x, xs, wp, wsc, out, M, K, N, ws, pdl, stream)
-               : gemm_launch(pl.g, x, xs, wp, wsc, out, M, K, N, ws, pdl, stream);
+                       int M, int K, int N, void* ws, bool pdl, cudaStream_t stream, int* acc, bool stall) {
+  return pl.tc ? tc_launch(pl.t, x, xs, wp, wsc, out, M, K, N, ws, pdl, stream, acc, stall)
+               : gemm_launch(pl.g, x, xs, wp, wsc, out, M, K, N, ws, pdl, stream, acc, stall);
 }
 
 }  // namespace w8a8
@@ -239,21 +239,37 @@ int w8a8_pack_weights(const int8_t* W, int K, int N, void* W_packed, void* ws, s
   return W8A8_OK;
 }
 
-int w8a8_gemm(const int8_t* x_q, const float* x_scale, const void* W_packed, const float* w_scale, void* out,
-              int M, int K, int N, int blocks, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
+// w8a8_gemm and w8a8_gemm_acc: every check, then the launch (acc may be NULL).
+static int gemm_call(const char* name, const int8_t* x_q, const float* x_scale, const void* W_packed,
+                     const float* w_scale, void* out, int32_t* acc, int M, int K, int N, int blocks, unsigned flags,
+                     void* ws, size_t ws_bytes, void* stream) {
   if (!x_q || !x_scale || !W_packed || !w_scale || !out || !ws) return W8A8_ERR_INVALID_ARG;
-  if (flags & ~(unsigned)W8A8_FLAG_PDL) return W8A8_ERR_INVALID_ARG;
+  if (flags & ~(unsigned)(W8A8_FLAG_PDL | W8A8_FLAG_TEST_STALL)) return W8A8_ERR_INVALID_ARG;
   AnyPlan pl;
   int rc = any_plan(M, K, N, blocks, device_sm_count(), &pl);
   if (rc != W8A8_OK) return rc;
   if (!aligned(x_q, 16) || !aligned(W_packed, 16) || !aligned(out, 16) || !aligned(x_scale, 4) ||
-      !aligned(w_scale, 4) || !aligned(ws, 256))
+      !aligned(w_scale, 4) || !aligned(ws, 256) || !aligned(acc, 4))
     return W8A8_ERR_MISALIGNED;
   if (ws_bytes < pl.workspace_bytes()) return W8A8_ERR_WORKSPACE_TOO_SMALL;
   cudaError_t e = any_launch(pl, x_q, x_scale, W_packed, w_scale, out, M, K, N, ws, (flags & W8A8_FLAG_PDL) != 0,
-                             static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "w8a8_gemm");
+                             static_cast<cudaStream_t>(stream), acc, (flags & W8A8_FLAG_TEST_STALL) != 0);
+  if (e != cudaSuccess) return cuda_fail(e, name);
   return W8A8_OK;
+}
+
+int w8a8_gemm(const int8_t* x_q, const float* x_scale, const void* W_packed, const float* w_scale, void* out,
+              int M, int K, int N, int blocks, unsigned flags, void* ws, size_t ws_bytes, void* stream) {
+  return gemm_call("w8a8_gemm", x_q, x_scale, W_packed, w_scale, out, nullptr, M, K, N, blocks, flags, ws, ws_bytes,
+                   stream);
+}
+
+int w8a8_gemm_acc(const int8_t* x_q, const float* x_scale, const void* W_packed, const float* w_scale, void* out,
+                  int32_t* acc, int M, int K, int N, int blocks, unsigned flags, void* ws, size_t ws_bytes,
+                  void* stream) {
+  if (!acc) return W8A8_ERR_INVALID_ARG;
+  return gemm_call("w8a8_gemm_acc", x_q, x_scale, W_packed, w_scale, out, acc, M, K, N, blocks, flags, ws, ws_bytes,
+                   stream);
 }
 
 size_t q8_0_workspace_bytes(int T_max, int K, int N) {

@@ -14,6 +14,10 @@ namespace w8a8 {
 // suspended poll (each poll sleeps at most kSuspendHintNs).
 constexpr long long kWaitTimeoutCycles = 2000000000ll;
 
+// The bound of the one wait that the W8A8_FLAG_TEST_STALL hook sets up to run out (a few
+// milliseconds at GB300 clocks), so that a test of the device fault path ends quickly.
+constexpr long long kTestStallCycles = 4000000ll;
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -61,16 +65,16 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t pa
 }
 
 // Wait for the phase of `parity` to complete.  Bounded: gives up when another thread of the CTA
-// has raised *abort, or after kWaitTimeoutCycles (then records the timeout in *status and raises
+// has raised *abort, or after `limit` cycles (then records the timeout in *status and raises
 // *abort).  Returns true when the phase completed.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint32_t* status) {
+                                          uint32_t* status, long long limit = kWaitTimeoutCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
     if (mbar_try_wait_suspend(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitTimeoutCycles) {
+    if (clock64() - t0 > limit) {
       atomicOr(status, W8A8_DEV_WAIT_TIMEOUT);
       *abort = 1;
       return false;

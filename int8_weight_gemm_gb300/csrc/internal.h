@@ -26,8 +26,11 @@ struct GemmPlan {
 };
 
 int gemm_plan(int M, int K, int N, int blocks, int sm_count, GemmPlan* plan);
+// acc (optional): the exact int32 sums [M, N] are stored there as well.  stall: the test hook of
+// W8A8_FLAG_TEST_STALL (one warp waits on a barrier that nothing completes, with a short bound).
 cudaError_t gemm_launch(const GemmPlan& pl, const int8_t* x, const float* xs, const void* wp, const float* wsc,
-                        void* out, int M, int K, int N, void* ws, bool pdl, cudaStream_t stream);
+                        void* out, int M, int K, int N, void* ws, bool pdl, cudaStream_t stream, int* acc = nullptr,
+                        bool stall = false);
 
 // M ranges of the two W8A8 arms: the register-fed decode kernel up to kDecodeMaxM rows, the
 // tensor-memory (tcgen05) kernel above it up to kTcMaxM.
@@ -46,7 +49,8 @@ struct TcPlan {
 
 int tc_plan(int M, int K, int N, int blocks, int sm_count, TcPlan* plan);
 cudaError_t tc_launch(const TcPlan& pl, const int8_t* x, const float* xs, const void* wp, const float* wsc, void* out,
-                      int M, int K, int N, void* ws, bool pdl, cudaStream_t stream);
+                      int M, int K, int N, void* ws, bool pdl, cudaStream_t stream, int* acc = nullptr,
+                      bool stall = false);
 
 // Either arm, chosen by M.
 struct AnyPlan {
@@ -58,7 +62,8 @@ struct AnyPlan {
 
 int any_plan(int M, int K, int N, int blocks, int sm_count, AnyPlan* plan);
 cudaError_t any_launch(const AnyPlan& pl, const int8_t* x, const float* xs, const void* wp, const float* wsc, void* out,
-                       int M, int K, int N, void* ws, bool pdl, cudaStream_t stream);
+                       int M, int K, int N, void* ws, bool pdl, cudaStream_t stream, int* acc = nullptr,
+                       bool stall = false);
 cudaError_t pack_launch(const int8_t* W, int K, int N, void* out, cudaStream_t stream);
 
 struct Q8Plan {

@@ -42,7 +42,9 @@ constexpr int kThreads = 32 * (kConsumerWarps + 2);   // + one producer warp + o
 // A launch whose CTAs each finish a single tile segment (the tile-aligned split) has nothing for
 // the combine warp to do and leaves it out.
 constexpr int kThreadsNoCombine = 32 * (kConsumerWarps + 1);
-constexpr int kFlushSlabs = 8;                     // 8 slabs of 32 k = 256 k per warp between int32 flushes
+// 16 slabs of 32 k = 512 k per warp between int32 flushes: a window's fp32 partial stays an exact
+// integer multiple of 2^-24 below 1 in magnitude (see offset_bytes_to_subnormal_pairs).
+constexpr int kFlushSlabs = 16;
 
 constexpr int kStageSlabs = 4;                     // one slab per consumer warp per stage
 
@@ -115,6 +117,8 @@ struct GemmParams {
   unsigned long long* tile_acc;
   int K;
   int pack_f;
+  int* acc_out;       // optional: the exact int32 sums [M, N] row-major, stored beside out
+  int debug_stall;    // test hook: one warp of CTA 0 waits on a barrier that nothing completes
 };
 
 // Walks a CTA's run of slabs [b0, b1) as stages of at most SS slabs that never cross a tile.
@@ -147,13 +151,23 @@ __device__ __forceinline__ int frag_index(int u, int j, int r, int lane) {
   return ((u * NT8 + j) * 4 + r) * 32 + lane;
 }
 
-// An fp32 value that is an integer v with |v| <= 2^22 (a partial sum over at most 256 k) to
-// int32 without the conversion unit: v + 1.5 * 2^23 lies in [2^23, 2^24], where fp32 spacing is
-// 1, so the sum is exact and its bit pattern is 0x4B400000 + v (at the ends 2^23 and 2^24 as
-// well).  One FP add and one integer add instead of a cvt, which runs at a quarter of the rate.
-__device__ __forceinline__ int exact_float_to_int(float v) {
-  return __float_as_int(__fadd_rn(v, 12582912.0f)) - 0x4B400000;
+// Weight operand.  The packed bytes are offset binary, b = w + 128 in [0, 255].  With a zero high
+// byte, the 16-bit pattern b is the fp16 subnormal b * 2^-24 (exponent field 0, significand b), so
+// one byte permute builds two MMA operands and nothing is subtracted: the MMA then sums
+// (w + 128) * x * 2^-24, and the 128 * sum_k x[m][k] it adds is taken off once per tile segment
+// from the activation sums (segment_total).  lo receives bytes (0, 2), hi bytes (1, 3), each as
+// (low half, high half).  Exactness: |(w + 128) x| <= 255 * 128 < 2^15, so a partial over at most
+// 512 k is a multiple of 2^-24 below 1 in magnitude; fp32 holds every such value exactly, and the
+// tensor pipe keeps fp16 subnormal operands (checked bit for bit on GB300 over 512-k windows at
+// both ends of the range).
+__device__ __forceinline__ void offset_bytes_to_subnormal_pairs(uint32_t u, uint32_t& lo, uint32_t& hi) {
+  lo = __byte_perm(u, 0u, 0x4240);
+  hi = __byte_perm(u, 0u, 0x4341);
 }
+
+// A window's fp32 partial (an integer multiple of 2^-24, below 1 in magnitude) as the int32
+// count of 2^-24 units: the scaling by 2^24 is exact and so is the conversion of an integral value.
+__device__ __forceinline__ int window_to_int(float v) { return __float2int_rn(__fmul_rn(v, 16777216.0f)); }
 
 // Split-tile combine words (see GemmParams::tile_acc).  Two-element word of f-bit fields: the
 // increment of one CTA's partials (a, b), and the decode of a word into the sums a, b of the
@@ -179,13 +193,15 @@ __device__ __forceinline__ int single_total(unsigned long long old, int v, uint3
   return (int)((uint32_t)old + ((uint32_t)v ^ 0x80000000u) - ((n & 1u) << 31));
 }
 
-// Epilogue of one output element: out[m][n] = bf16_rne((float(acc) * x_scale[m]) * w_scale[n]).
+// Epilogue of one output element: out[m][n] = bf16_rne((float(acc) * x_scale[m]) * w_scale[n]),
+// and the int32 sum itself when the caller asked for it.
 __device__ __forceinline__ void store_out(const GemmParams& p, int m, int n, int acc, float xsv, float wsv) {
   if (m < p.M && n < p.N) {
     float f = __int2float_rn(acc);
     f = __fmul_rn(f, xsv);
     f = __fmul_rn(f, wsv);
     p.out[(long long)m * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(f));
+    if (p.acc_out) p.acc_out[(long long)m * p.N + n] = acc;
   }
 }
 
@@ -214,9 +230,11 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
   __shared__ __align__(8) uint64_t empty_bar[NS];  // the stage's consumer warps took their slabs
   __shared__ float xs_sm[32];                      // x_scale (0 past M)
   __shared__ float ws_sm[2][kTileRows];            // w_scale of a segment's tile, by segment parity
+  __shared__ int xsum_sm[2][32];                   // sum_k x[m][k] over a segment's k, by segment parity
   __shared__ __align__(8) uint64_t seg_bar;        // every consumer warp finished the CTA's last segment
   __shared__ __align__(8) uint64_t seg_full[2];    // every consumer warp flushed an earlier segment (by parity)
   __shared__ __align__(8) uint64_t seg_free[2];    // the combine warp is done with that segment's buffer
+  __shared__ __align__(8) uint64_t stall_bar;      // test hook only: never completed
   __shared__ int abort_flag;
 
   // 128B-swizzled TMA boxes need a 1 KiB aligned destination.
@@ -251,6 +269,7 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
     mbar_init(&seg_full[1], kConsumerWarps);
     mbar_init(&seg_free[0], 1);
     mbar_init(&seg_free[1], 1);
+    mbar_init(&stall_bar, 1);
     abort_flag = 0;
     mbar_fence_init();
     // The packed weight is never written by the work this call depends on, so its first stages
@@ -263,15 +282,21 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
     }
   }
   for (int i = threadIdx.x; i < L::kSegSumInts; i += (kMulti ? kThreads : kThreadsNoCombine)) segsum[i] = 0;
+  if (threadIdx.x < 64) (&xsum_sm[0][0])[threadIdx.x] = 0;
   __syncthreads();
   pdl_trigger();   // the next call on the stream may start its own weight prefetch
 
-  // Element e of a segment's sums (layout [sub][j][r][lane]) of tile t, its scales parked in
-  // buffer b: its row m and column n are the inverse of frag_index and of the accumulator fragment
-  // (lane = 4g + c holds rows 2c + (r & 1) of n8 tile j and columns g + 8 (r >> 1) of sub-tile u).
+  // Row m of element e of a segment's sums (layout [sub][j][r][lane]) and its column inside the
+  // tile: the inverse of frag_index and of the accumulator fragment (lane = 4g + c holds rows
+  // 2c + (r & 1) of n8 tile j and columns g + 8 (r >> 1) of sub-tile u).
+  auto elem_m = [](int e) { return 8 * ((e >> 7) % NT8) + 2 * (e & 3) + ((e >> 5) & 1); };
+  auto elem_n = [](int e) { return 16 * ((e >> 7) / NT8) + ((e & 31) >> 2) + 8 * ((e >> 6) & 1); };
+  // The exact int32 sum of element e over this CTA's part of the segment in buffer b: the shared
+  // sum holds sum (w + 128) x, and 128 * sum_k x[m][k] over the segment's k comes off here.
+  auto segment_total = [&](int e, int b, int biased) { return biased - 128 * xsum_sm[b][elem_m(e)]; };
+  // Store element e of tile t with its scales parked in buffer b.
   auto store_elem = [&](int e, int t, int b, int total) {
-    const int m = 8 * ((e >> 7) % NT8) + 2 * (e & 3) + ((e >> 5) & 1);
-    const int nl = 16 * ((e >> 7) / NT8) + ((e & 31) >> 2) + 8 * ((e >> 6) & 1);
+    const int m = elem_m(e), nl = elem_n(e);
     store_out(p, m, t * kTileRows + nl, total, xs_sm[m], ws_sm[b][nl]);
   };
 
@@ -284,18 +309,23 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
       for (int j = 0; j < pq; pre.next(), ++j)
         tma_load_2d(xraw + j * L::kXRawStage, &p.xmap, pre.kb0() * kKBlock, 0, &full_bar[j]);
     }
+    int s = pq % NS;                       // ring slot of stage pq
+    uint32_t ph = (uint32_t)((pq / NS) & 1);   // its phase parity
     for (; !it.done(); it.next(), ++pq) {
-      const int s = pq % NS;
-      if (!mbar_wait(&empty_bar[s], ((pq / NS) & 1) ^ 1, &abort_flag, p.status)) break;
+      if (!mbar_wait(&empty_bar[s], ph ^ 1u, &abort_flag, p.status)) break;
       mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(it.ns * kSlabBytes) + xbox);
       bulk_g2s_hint(wring + s * L::kWStage, p.wp + (size_t)it.u * kSlabBytes, (uint32_t)(it.ns * kSlabBytes), &full_bar[s],
                     policy);
       tma_load_2d(xraw + s * L::kXRawStage, &p.xmap, it.kb0() * kKBlock, 0, &full_bar[s]);
+      if (++s == NS) {
+        s = 0;
+        ph ^= 1u;
+      }
     }
     // Drain: every copy this thread issued must land before the CTA may exit.
-    for (int s = 0; s < NS && s < pq; ++s) {
-      const int last = s + NS * ((pq - 1 - s) / NS);
-      mbar_wait_drain(&full_bar[s], (uint32_t)((last / NS) & 1), p.status);
+    for (int d = 0; d < NS && d < pq; ++d) {
+      const int last = d + NS * ((pq - 1 - d) / NS);
+      mbar_wait_drain(&full_bar[d], (uint32_t)((last / NS) & 1), p.status);
     }
     return;
   }
@@ -320,7 +350,7 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
       const uint32_t n = (uint32_t)gemm_split_contributors(p.split, t);
       if (seg_begin == t * p.KB) {   // the whole tile is ours (it ends before b1, so it is complete)
         for (int e = lane; e < kSegInts; e += 32) {
-          store_elem(e, t, buf, sums[e]);
+          store_elem(e, t, buf, segment_total(e, buf, sums[e]));
           sums[e] = 0;
         }
       } else if (p.pack_f) {
@@ -330,7 +360,10 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const int i = lane + 32 * (w0 + k);
-            if (w0 + k < kWords) old[k] = atom_add_relaxed_u64(tacc + i, pair_increment(sums[i], sums[i + kHalf], p.pack_f));
+            if (w0 + k < kWords)
+              old[k] = atom_add_relaxed_u64(tacc + i, pair_increment(segment_total(i, buf, sums[i]),
+                                                                     segment_total(i + kHalf, buf, sums[i + kHalf]),
+                                                                     p.pack_f));
           }
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
@@ -340,8 +373,8 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
             const uint32_t arrived = pair_decode(old[k], p.pack_f, &a, &bb);
             if (arrived == n - 1) {
               tacc[i] = 0ull;
-              store_elem(i, t, buf, (int)(a + sums[i]));
-              store_elem(i + kHalf, t, buf, (int)(bb + sums[i + kHalf]));
+              store_elem(i, t, buf, (int)(a + segment_total(i, buf, sums[i])));
+              store_elem(i + kHalf, t, buf, (int)(bb + segment_total(i + kHalf, buf, sums[i + kHalf])));
             } else if (arrived >= n) {
               atomicOr(p.status, W8A8_DEV_COUNTER_CORRUPT);
             }
@@ -356,7 +389,7 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const int e = lane + 32 * (w0 + k);
-            if (w0 + k < kElems) old[k] = atom_add_relaxed_u64(tacc + e, single_increment(sums[e]));
+            if (w0 + k < kElems) old[k] = atom_add_relaxed_u64(tacc + e, single_increment(segment_total(e, buf, sums[e])));
           }
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
@@ -365,7 +398,7 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
             const uint32_t arrived = (uint32_t)(old[k] >> 52);
             if (arrived == n - 1) {
               tacc[e] = 0ull;
-              store_elem(e, t, buf, single_total(old[k], sums[e], n));
+              store_elem(e, t, buf, single_total(old[k], segment_total(e, buf, sums[e]), n));
             } else if (arrived >= n) {
               atomicOr(p.status, W8A8_DEV_COUNTER_CORRUPT);
             }
@@ -373,6 +406,8 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
           }
         }
       }
+      __syncwarp();
+      xsum_sm[buf][lane] = 0;   // every lane has read the activation sums of this buffer
       __syncwarp();
       if (lane == 0) mbar_arrive(&seg_free[buf]);
     }
@@ -382,16 +417,27 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
   // ---------------------------------------------------------------- consumer warps
   // Warp w multiplies slab (w % 4) of every stage of parity (w / 4), covering all four 16-row
   // sub-tiles of the 64-row tile.  Each warp converts only its own 32-k activation slice, so the
-  // warps never wait for one another inside a tile.  Their fp32 partials (exact integers) are
-  // flushed as int32 into the segment's shared sum buffer (two buffers, used by alternate
-  // segments).  At the end of each segment all consumer threads finish it together: every thread
-  // takes kPer of its output elements (one returning atomic each for a split tile), so the tail
-  // of a segment is one global round trip.  Meanwhile the producer keeps filling the ring.
+  // warps never wait for one another inside a tile.  Their fp32 partials (exact) are flushed as
+  // int32 into the segment's shared sum buffer (two buffers, used by alternate segments), and the
+  // lanes' activation sums go to the segment's xsum_sm.  At the end of each segment all consumer
+  // threads finish it together: every thread takes kPer of its output elements (one returning
+  // atomic each for a split tile), so the tail of a segment is one global round trip.  Meanwhile
+  // the producer keeps filling the ring.
   pdl_wait();   // x_scale, w_scale, out and the accumulators may belong to the previous call
+  if (p.debug_stall && blockIdx.x == 0 && warp == 0) {
+    // Test hook of the device fault path: this warp waits, with a short bound, on a barrier that
+    // nothing completes.  The wait runs out, records W8A8_DEV_WAIT_TIMEOUT and raises the abort
+    // flag; the other roles of the CTA then give up at their next wait, the producer after
+    // draining the copies it issued.  Nothing hangs and nothing faults.
+    mbar_wait(&stall_bar, 0u, &abort_flag, p.status, kTestStallCycles);
+    return;
+  }
   const int g = lane >> 2, c = lane & 3;
   const int slab = warp & (kStageSlabs - 1);
   const int half = warp / kStageSlabs;
   const int sub0 = kHalfSubTiles ? kWarpSubTiles * half : 0;   // first sub-tile of this warp
+  // The activation sums: warps of one slab position share its activations, so one of them adds.
+  const bool sums_x = !kHalfSubTiles || half == 0;
   float facc[kWarpSubTiles][NT8][4];
 #pragma unroll
   for (int u = 0; u < kWarpSubTiles; ++u)
@@ -399,6 +445,9 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
     for (int j = 0; j < NT8; ++j)
 #pragma unroll
       for (int r = 0; r < 4; ++r) facc[u][j][r] = 0.f;
+  int xsum[NT8];          // sum of this lane's activation bytes of row 8j + g over the segment
+#pragma unroll
+  for (int j = 0; j < NT8; ++j) xsum[j] = 0;
   int since = 0;          // slabs accumulated in fp32 by this warp since its last flush
   int segs = 0;
   int q = 0;              // CTA-wide stage index of the current segment's first stage
@@ -409,7 +458,7 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
   // once, were measured to stall the epilogue for microseconds.
   const float xs_reg = threadIdx.x < 32 && (int)threadIdx.x < p.M ? __ldg(p.x_scale + threadIdx.x) : 0.f;
   float ws_reg = 0.f;
-  // Add this warp's fp32 partial sums (exact integers) into the segment's shared int32 sums.
+  // Add this warp's fp32 window partials (exact) into the segment's shared int32 sums.
   auto flush = [&](int* dst) {
 #pragma unroll
     for (int u = 0; u < kWarpSubTiles; ++u)
@@ -417,7 +466,7 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
       for (int j = 0; j < NT8; ++j)
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          atomicAdd(dst + frag_index<NT8>(sub0 + u, j, r, lane), exact_float_to_int(facc[u][j][r]));
+          atomicAdd(dst + frag_index<NT8>(sub0 + u, j, r, lane), window_to_int(facc[u][j][r]));
           facc[u][j][r] = 0.f;
         }
   };
@@ -434,7 +483,11 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
 
   // The run [b0, b1) is walked segment by segment (one tile's part each); a segment of n slabs is
   // ceil(n / 4) stages of the CTA-wide stage sequence, the last one possibly partial.  q is the
-  // CTA-wide index of the segment's first stage; this warp visits only its own stages.
+  // CTA-wide index of the segment's first stage; this warp visits only its own stages nq, whose
+  // ring slot and phase parity it keeps up to date as it goes.
+  int nq = kHalfSubTiles ? 0 : half;   // next CTA-wide stage this warp visits (< NS here)
+  int slot = nq;
+  uint32_t phase = 0;
   for (int seg_begin = b0, seg_end = 0; seg_begin < b1; seg_begin = seg_end) {
     const int t = seg_begin / p.KB;
     seg_end = min(b1, (t + 1) * p.KB);
@@ -450,26 +503,26 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
       const int n = t * kTileRows + (int)threadIdx.x;
       ws_reg = n < p.N ? __ldg(p.w_scale + n) : 0.f;
     }
-    for (int i = kHalfSubTiles ? 0 : ((half - q) & 1); i < seg_stages; i += kStep) {
-      const int qs = q + i;
-      const int s = qs % NS;
-      if (!mbar_wait(&full_bar[s], (uint32_t)((qs / NS) & 1), &abort_flag, p.status)) return;
-      if (slab < seg_slabs - kStageSlabs * i) {
+    const int q_end = q + seg_stages;
+    for (; nq < q_end; nq += kStep) {
+      if (!mbar_wait(&full_bar[slot], phase, &abort_flag, p.status)) return;
+      if (slab < seg_slabs - kStageSlabs * (nq - q)) {
         // Weight fragments of this warp's sub-tiles, then this slab's activation B fragments.
-        const uint8_t* wst = wring + s * L::kWStage + w_off;
+        const uint8_t* wst = wring + slot * L::kWStage + w_off;
         uint4 w[kWarpSubTiles];
 #pragma unroll
         for (int u = 0; u < kWarpSubTiles; ++u) w[u] = *reinterpret_cast<const uint4*>(wst + u * 512);
-        const uint8_t* xr = xraw + s * L::kXRawStage + x_off;
+        const uint8_t* xr = xraw + slot * L::kXRawStage + x_off;
         uint32_t b[NT8][4];
 #pragma unroll
         for (int j = 0; j < NT8; ++j) {
           const uint2 v = *reinterpret_cast<const uint2*>(xr + j * 1024);
           offset_bytes_to_half2(v.x ^ 0x80808080u, b[j][0], b[j][1]);
           offset_bytes_to_half2(v.y ^ 0x80808080u, b[j][2], b[j][3]);
+          if (sums_x) xsum[j] = __dp4a((int)v.y, 0x01010101, __dp4a((int)v.x, 0x01010101, xsum[j]));
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[s]);   // registers hold everything this warp needs
+        if (lane == 0) mbar_arrive(&empty_bar[slot]);   // registers hold everything this warp needs
         if (since == kFlushSlabs) {
           flush(segsum + (segs & 1) * kSegInts);
           since = 0;
@@ -479,10 +532,10 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
         uint32_t a[kWarpSubTiles][2][4];
 #pragma unroll
         for (int u = 0; u < kWarpSubTiles; ++u) {
-          offset_bytes_to_half2(w[u].x, a[u][0][0], a[u][0][2]);   // row g,   k 8c+0..3
-          offset_bytes_to_half2(w[u].y, a[u][0][1], a[u][0][3]);   // row g+8, k 8c+0..3
-          offset_bytes_to_half2(w[u].z, a[u][1][0], a[u][1][2]);   // row g,   k 8c+4..7
-          offset_bytes_to_half2(w[u].w, a[u][1][1], a[u][1][3]);   // row g+8, k 8c+4..7
+          offset_bytes_to_subnormal_pairs(w[u].x, a[u][0][0], a[u][0][2]);   // row g,   k 8c+0..3
+          offset_bytes_to_subnormal_pairs(w[u].y, a[u][0][1], a[u][0][3]);   // row g+8, k 8c+0..3
+          offset_bytes_to_subnormal_pairs(w[u].z, a[u][1][0], a[u][1][2]);   // row g,   k 8c+4..7
+          offset_bytes_to_subnormal_pairs(w[u].w, a[u][1][1], a[u][1][3]);   // row g+8, k 8c+4..7
         }
 #pragma unroll
         for (int st = 0; st < 2; ++st)
@@ -495,10 +548,15 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
         ++since;
       } else {
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[s]);
+        if (lane == 0) mbar_arrive(&empty_bar[slot]);
+      }
+      slot += kStep;
+      if (slot >= NS) {
+        slot -= NS;
+        phase ^= 1u;
       }
     }
-    q += seg_stages;
+    q = q_end;
 
     // ------------------------------------------------------------ end of this CTA's part of a tile
     const int buf = segs & 1;
@@ -507,6 +565,17 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
     int* const sums = segsum + buf * kSegInts;
     if (since) flush(sums);
     since = 0;
+    if (sums_x) {
+      // Row 8j + g's activation sum over this warp's slabs: the four lanes of a row hold 32 k each.
+#pragma unroll
+      for (int j = 0; j < NT8; ++j) {
+        int sx = xsum[j];
+        sx += __shfl_xor_sync(0xffffffffu, sx, 1);
+        sx += __shfl_xor_sync(0xffffffffu, sx, 2);
+        if (c == 0) atomicAdd(&xsum_sm[buf][8 * j + g], sx);
+        xsum[j] = 0;
+      }
+    }
     ++segs;
     if (kMulti && seg_end != b1) {
       // An earlier segment: hand it to the combine warp and stream on.
@@ -522,9 +591,10 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
     if (lane == 0) mbar_arrive(&seg_bar);
     if (!mbar_wait(&seg_bar, 0u, &abort_flag, p.status)) return;
     int* const mine = sums + threadIdx.x;   // element i at mine[kConsumerThreads * i]
+    auto mine_total = [&](int i) { return segment_total(threadIdx.x + kConsumerThreads * i, buf, mine[kConsumerThreads * i]); };
     if (seg_begin == t * p.KB && seg_end == (t + 1) * p.KB) {   // the whole tile is ours
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) finish(i, t, buf, mine[kConsumerThreads * i]);
+      for (int i = 0; i < kPer; ++i) finish(i, t, buf, mine_total(i));
       break;
     }
     // Split tile.  Each contributor adds its partials into the elements' workspace words with one
@@ -539,15 +609,15 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
 #pragma unroll
       for (int i = 0; i < kPer / 2; ++i)
         old[i] = atom_add_relaxed_u64(tacc + kConsumerThreads * i,
-                                      pair_increment(mine[kConsumerThreads * i], mine[kConsumerThreads * (i + kPer / 2)], p.pack_f));
+                                      pair_increment(mine_total(i), mine_total(i + kPer / 2), p.pack_f));
 #pragma unroll
       for (int i = 0; i < kPer / 2; ++i) {
         long long a, bb;
         const uint32_t arrived = pair_decode(old[i], p.pack_f, &a, &bb);
         if (arrived == arrivals - 1) {
           tacc[kConsumerThreads * i] = 0ull;
-          finish(i, t, buf, (int)(a + mine[kConsumerThreads * i]));
-          finish(i + kPer / 2, t, buf, (int)(bb + mine[kConsumerThreads * (i + kPer / 2)]));
+          finish(i, t, buf, (int)(a + mine_total(i)));
+          finish(i + kPer / 2, t, buf, (int)(bb + mine_total(i + kPer / 2)));
         } else if (arrived >= arrivals) {
           atomicOr(p.status, W8A8_DEV_COUNTER_CORRUPT);
         }
@@ -555,13 +625,13 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
     } else {
       unsigned long long old[kPer];
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) old[i] = atom_add_relaxed_u64(tacc + kConsumerThreads * i, single_increment(mine[kConsumerThreads * i]));
+      for (int i = 0; i < kPer; ++i) old[i] = atom_add_relaxed_u64(tacc + kConsumerThreads * i, single_increment(mine_total(i)));
 #pragma unroll
       for (int i = 0; i < kPer; ++i) {
         const uint32_t arrived = (uint32_t)(old[i] >> 52);
         if (arrived == arrivals - 1) {
           tacc[kConsumerThreads * i] = 0ull;
-          finish(i, t, buf, single_total(old[i], mine[kConsumerThreads * i], arrivals));
+          finish(i, t, buf, single_total(old[i], mine_total(i), arrivals));
         } else if (arrived >= arrivals) {
           atomicOr(p.status, W8A8_DEV_COUNTER_CORRUPT);
         }
@@ -663,7 +733,7 @@ static cudaError_t launch_gemm(const GemmParams& p, int blocks, int threads, boo
 }
 
 cudaError_t gemm_launch(const GemmPlan& pl, const int8_t* x, const float* xs, const void* wp, const float* wsc,
-                        void* out, int M, int K, int N, void* ws, bool pdl, cudaStream_t stream) {
+                        void* out, int M, int K, int N, void* ws, bool pdl, cudaStream_t stream, int* acc, bool stall) {
   GemmParams p;
   // Activation tensor map: [M rows, K bytes], box of 128 bytes x 8*NT8 rows (rows >= M read as 0).
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
@@ -686,6 +756,8 @@ cudaError_t gemm_launch(const GemmPlan& pl, const int8_t* x, const float* xs, co
   p.split = make_gemm_split(pl.n_tiles, pl.kb, pl.blocks);
   p.pack_f = pl.pack_f;
   p.pdl = pdl ? 1 : 0;
+  p.acc_out = acc;
+  p.debug_stall = stall ? 1 : 0;
   const bool multi = pl.threads == kThreads;
   switch (pl.nt8) {
     case 1: return multi ? launch_gemm<1, kStages1, true>(p, pl.blocks, pl.threads, pdl, stream)

@@ -106,6 +106,8 @@ struct TcParams {
   int* planes;          // [tile][m < N_mma][row < 128] int32 sums of a split tile, zero between calls
   GemmSplit split;      // over the 128-row tiles, in 32-k units
   int M, N, KB, tiles64;
+  int* acc_out;         // optional: the exact int32 sums [M, N] row-major, stored beside out
+  int debug_stall;      // test hook: one converter warp of CTA 0 waits on a barrier that nothing completes
 };
 
 // The CTA's schedule: its run of units [b0, b1) is a sequence of segments (one tile's part each),
@@ -188,7 +190,8 @@ __device__ __forceinline__ uint16_t epilogue(int acc, float xsv, float wsv) {
 // raised *abort, or after kWaitTimeoutCycles (then records the timeout in *status and raises
 // *abort).  Returns true when the phase completed.
 constexpr unsigned kPollSleepNs = 32;
-__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* status) {
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* status,
+                                        long long limit = kWaitTimeoutCycles) {
   const long long t0 = clock64();
   for (int n = 0;; ++n) {
     uint32_t done;
@@ -201,7 +204,7 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile
     __nanosleep(kPollSleepNs);
     if ((n & 63) == 63) {
       if (*abort) return false;
-      if (clock64() - t0 > kWaitTimeoutCycles) {
+      if (clock64() - t0 > limit) {
         atomicOr(status, W8A8_DEV_WAIT_TIMEOUT);
         *abort = 1;
         return false;
@@ -222,9 +225,10 @@ __device__ __forceinline__ bool mbar_wait_all(uint64_t* bar, uint32_t parity, vo
 // Bounded wait on one phase of `bar` for a whole warp: lane 0 polls, the other lanes wait for it at
 // the warp barrier of the broadcast; the outcome is the same for all 32 lanes.  For waits whose next
 // step is a tensor-memory instruction behind tcgen05.fence::after_thread_sync.
-__device__ __forceinline__ bool mbar_wait_lane0(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* status) {
+__device__ __forceinline__ bool mbar_wait_lane0(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* status,
+                                                long long limit = kWaitTimeoutCycles) {
   int ok = 0;
-  if ((threadIdx.x & 31) == 0) ok = tc_wait(bar, parity, abort, status) ? 1 : 0;
+  if ((threadIdx.x & 31) == 0) ok = tc_wait(bar, parity, abort, status, limit) ? 1 : 0;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
@@ -296,6 +300,7 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
   __shared__ __align__(8) uint64_t dempty_bar[2];   // an accumulator buffer has been read out
   __shared__ __align__(8) uint64_t final_bar[kI];   // every MMA of an issuer completed
   __shared__ __align__(8) uint64_t sync_bar;        // converter warps meet at a split tile's combine
+  __shared__ __align__(8) uint64_t stall_bar;       // test hook only: never completed
   __shared__ uint32_t tmem_base;
   __shared__ float xs_sm[kN];
   __shared__ int abort_flag;
@@ -328,6 +333,7 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
 #pragma unroll
     for (int i = 0; i < kI; ++i) mbar_init(&final_bar[i], 1);
     mbar_init(&sync_bar, kConvWarps);
+    mbar_init(&stall_bar, 1);
     abort_flag = 0;
     mbar_fence_init();
   }
@@ -480,7 +486,10 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
             if (n < p.N) {
 #pragma unroll
               for (int c = 0; c < L::kCols; ++c, o += p.N)
-                if (c < mrows) *o = epilogue(iacc[c], xs_sm[m0 + c], wsv);
+                if (c < mrows) {
+                  *o = epilogue(iacc[c], xs_sm[m0 + c], wsv);
+                  if (p.acc_out) p.acc_out[(size_t)(m0 + c) * p.N + n] = iacc[c];
+                }
             }
           } else {
             // Split tile: add this partial to the tile's int32 plane, count the arrival (one thread,
@@ -512,6 +521,7 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
                     const int total = ld_relaxed_s32(w);
                     *w = 0;
                     *o = epilogue(total, xs_sm[m0 + c], wsv);
+                    if (p.acc_out) p.acc_out[(size_t)(m0 + c) * p.N + n] = total;
                   }
                 }
               }
@@ -526,6 +536,16 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
     };
 
     bool ok = true;
+    if (p.debug_stall && blockIdx.x == 0 && warp == 0) {
+      // Test hook of the device fault path (after the converter warps' named barrier, which every
+      // one of them must reach): this warp waits, with a short bound, on a barrier that nothing
+      // completes.  The wait runs out, records W8A8_DEV_WAIT_TIMEOUT and raises the abort flag;
+      // every other role gives up at its next wait, the issuers after their MMAs have completed and
+      // the producers after their copies have landed, and all meet at the final barrier before the
+      // tensor memory is freed.
+      mbar_wait_lane0(&stall_bar, 0u, &abort_flag, p.status, kTestStallCycles);
+      ok = false;
+    }
     for (Walk it(b0, b1, p.KB); ok && !it.done(); it.next()) {
       const int s = it.q % NW;
       const int a = it.q % NA;
@@ -684,7 +704,7 @@ int tc_plan(int M, int K, int N, int blocks, int sm_count, TcPlan* plan) {
 }
 
 cudaError_t tc_launch(const TcPlan& pl, const int8_t* x, const float* xs, const void* wp, const float* wsc, void* out,
-                      int M, int K, int N, void* ws, bool pdl, cudaStream_t stream) {
+                      int M, int K, int N, void* ws, bool pdl, cudaStream_t stream, int* acc, bool stall) {
   uint8_t* const w = static_cast<uint8_t*>(ws);
   void* const x16 = w + pl.x16_offset;
   tc::TcParams p;
@@ -709,6 +729,8 @@ cudaError_t tc_launch(const TcPlan& pl, const int8_t* x, const float* xs, const 
   p.N = N;
   p.KB = pl.kb;
   p.tiles64 = pl.tiles64;
+  p.acc_out = acc;
+  p.debug_stall = stall ? 1 : 0;
   e = tc::launch_x16(x, x16, (long long)M * K / 32, pdl, stream);
   if (e != cudaSuccess) return e;
   return pl.mma_n == 64 ? tc::launch_tc<4>(p, pl.blocks, stream) : tc::launch_tc<8>(p, pl.blocks, stream);

@@ -15,7 +15,7 @@
  *         row's fp16 scales); the parity test's FP64 reference computed from the very Q8_0
  *         bytes the kernel reads.
  *
- * Readings where the pages leave a step open (also listed in the design notes):
+ * Readings where the pages leave a step open (the plainest reading the rest of the pages support):
  *  - The W8A8 epilogue is (float(acc) * x_scale[m]) * w_scale[n], each step an IEEE fp32
  *    multiply rounded to nearest even, then rounded to nearest even into bfloat16.  The pages
  *    only say "scales ... bf16"; the library's interface defines this order, x_scale first.
@@ -193,7 +193,7 @@ void oracle_q8_0_norms(const uint16_t* x, const int8_t* q, const uint16_t* d,
 
 /* Q8_0 read with an RMS-norm prologue.  [Q8_0] section "What changed": the down kernel stages
  * R' * w_norm unscaled together with the sums of squares of the rows, and the last work-group to
- * arrive applies rs per stream.  Generic reading (the design notes list it): rs[t] is the inverse
+ * arrive applies rs per stream; the page does not define rs.  Generic reading: rs[t] is the inverse
  * root mean square of x's row t, 1 / sqrt(sum_k x[t][k]^2 / K + eps), and
  *   y[t][n] = rs[t] * sum_k (x[t][k] * g[k]) * (d[n][k/32] * q[n][k]),
  * all in double from the very bf16 / fp16 / int8 bytes the kernel reads.  x: bf16 bits [T,K];

@@ -28,5 +28,10 @@ class W8A8Case:
         return lib8.w8a8_gemm(self.x, self.xs, self.Wp, self.ws_scale, self.ws, self.N, out=out,
                               blocks=self.blocks if blocks is None else blocks, flags=flags)
 
+    def run_acc(self, blocks=None, flags=0):
+        """The same call through w8a8_gemm_acc: (out bf16, acc int32) as device tensors."""
+        return lib8.w8a8_gemm_acc(self.x, self.xs, self.Wp, self.ws_scale, self.ws, self.N,
+                                  blocks=self.blocks if blocks is None else blocks, flags=flags)
+
     def status(self):
         return lib8.w8a8_workspace_status(self.ws)

@@ -333,18 +333,22 @@ def test_misaligned_and_short_workspace_are_rejected_on_the_host():
 def _frag_a(words):
     """mma.m16n8k16 A fragment of one lane from the kernel's conversion of 4 packed words.
 
-    Each word's bytes (0,2) form one register and bytes (1,3) another (as offset_bytes_to_half2).
-    Registers a0..a3 of one k16 step are (row g, slots 2c,2c+1), (row g+8, ...), (row g, slots
-    2c+8,2c+9), (row g+8, ...) per the PTX fragment layout; the kernel feeds
+    Each word's bytes (0,2) form one register and bytes (1,3) another (as
+    offset_bytes_to_subnormal_pairs): a byte b of the packed weight (offset binary, b = w + 128)
+    becomes the fp16 subnormal b * 2^-24, so the fragment carries the unsigned bytes themselves, in
+    units of 2^-24.  Registers a0..a3 of one k16 step are (row g, slots 2c,2c+1), (row g+8, ...),
+    (row g, slots 2c+8,2c+9), (row g+8, ...) per the PTX fragment layout; the kernel feeds
     {lo(w_row_g), lo(w_row_g8), hi(w_row_g), hi(w_row_g8)}."""
     def lohi(w):
-        b = [((w >> (8 * i)) & 0xFF) ^ 0x80 for i in range(4)]
-        b = [v - 256 if v >= 128 else v for v in b]
+        b = [(w >> (8 * i)) & 0xFF for i in range(4)]
         return (b[0], b[2]), (b[1], b[3])
     return [lohi(w) for w in words]
 
 
 def test_emulated_fragment_path_reproduces_x_at_w():
+    """The MMA sums (w + 128) * x in units of 2^-24; the activation sums that the lanes gather
+    with dp4a (each lane 8 bytes of row 8j + g per slab, the four lanes of a row 32 k) take
+    128 * sum_k x off once, which leaves exactly x @ W."""
     M, K, N = 12, 64, 128
     x, _, W, _ = synth.w8a8_inputs(M, K, N, seed=21)
     packed = oracle.w8a8_pack(W)
@@ -374,6 +378,15 @@ def test_emulated_fragment_path_reproduces_x_at_w():
                             n = 64 * t + 16 * s + row
                             for slot, a in slots.items():
                                 acc[n, :] += a * xp[:, slot_k[slot]]
+    # the lanes' activation sums: lane (g, c) adds bytes k = 32 kb + 8c ... 8c + 7 of row 8j + g
+    xsum = np.zeros(8 * NT8, dtype=np.int64)
+    for kb in range(KB):
+        for g in range(8):
+            for c in range(4):
+                for j in range(NT8):
+                    xsum[8 * j + g] += int(xp[8 * j + g, 32 * kb + 8 * c: 32 * kb + 8 * c + 8].sum())
+    assert np.array_equal(xsum, xp.sum(axis=1))
+    acc -= 128 * xsum[None, :]
     ref = oracle.w8a8_acc(x, W)
     np.testing.assert_array_equal(acc[:N, :M].T, ref)
 

@@ -48,7 +48,22 @@ def test_reference_arm_prints_one_contract_line():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == out["value"] and cb["sample"]
     assert out["e2e"] == {"value": out["value"], "unit": out["unit"], "h2d_bytes_per_step": 0,
                           "d2h_bytes_per_step": 0}
-    assert out["config"]["workload"]
+    assert out["config"] == bench.workload_config(bench.HEADLINE, 1)   # the device arm's config, exactly
+    assert str(bench.DEFAULT["N"]) in cb["sample"] and "whole" in cb["sample"]
+
+
+def test_oracle_on_cores_equals_one_whole_oracle_call():
+    import numpy as np
+
+    import oracle
+    import synth
+
+    x, xs, W, ws = synth.w8a8_inputs(5, 256, 200, seed=8, dist="mlp")
+    par = bench.OracleOnCores(x, xs, W, ws, threads=4)
+    try:
+        np.testing.assert_array_equal(par.call(), oracle.w8a8_gemm(x, xs, W, ws))
+    finally:
+        par.close()
 
 
 def test_device_arm_fails_loudly_without_a_gpu():

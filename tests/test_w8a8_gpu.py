@@ -1,4 +1,5 @@
-"""W8A8 decode GEMM on the GPU against the oracle: bit-exact bf16 outputs on every case.
+"""W8A8 decode GEMM on the GPU against the oracle: bit-exact bf16 outputs and int32 accumulators
+(through w8a8_gemm_acc) on every case.
 
 Cases: the five workload families (seeded, full size, compared element by element), ragged
 shapes (M not a multiple of 8, N not a multiple of 64), every split count class (one CTA, a few,
@@ -19,12 +20,21 @@ pytestmark = pytest.mark.gpu
 
 
 def _check(case, x, xs, W, ws, blocks=None):
+    """bf16 outputs of w8a8_gemm, and both the outputs and the int32 accumulators of
+    w8a8_gemm_acc, bit for bit against the oracle."""
     ref = oracle.w8a8_gemm(x, xs, W, ws)
     out = case.run(blocks=blocks)
     torch.cuda.synchronize()
     got = bf16_bits(out)
     mism = np.count_nonzero(got != ref)
     assert mism == 0, f"{mism} of {ref.size} outputs differ"
+    assert case.status() == 0
+    out2, acc = case.run_acc(blocks=blocks)
+    torch.cuda.synchronize()
+    ref_acc = oracle.w8a8_acc(x, W)
+    acc_mism = np.count_nonzero(acc.cpu().numpy().astype(np.int64) != ref_acc)
+    assert acc_mism == 0, f"{acc_mism} of {ref_acc.size} int32 accumulators differ"
+    assert np.array_equal(bf16_bits(out2), ref)
     assert case.status() == 0
 
 

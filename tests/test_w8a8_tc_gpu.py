@@ -28,12 +28,21 @@ def _zeroed_end(N):
 
 
 def _check(case, x, xs, W, ws, blocks=None):
+    """bf16 outputs of w8a8_gemm, and both the outputs and the int32 accumulators of
+    w8a8_gemm_acc, bit for bit against the oracle."""
     ref = oracle.w8a8_gemm(x, xs, W, ws)
     out = case.run(blocks=blocks)
     torch.cuda.synchronize()
     got = bf16_bits(out)
     mism = np.count_nonzero(got != ref)
     assert mism == 0, f"{mism} of {ref.size} outputs differ"
+    assert case.status() == 0
+    out2, acc = case.run_acc(blocks=blocks)
+    torch.cuda.synchronize()
+    ref_acc = oracle.w8a8_acc(x, W)
+    acc_mism = np.count_nonzero(acc.cpu().numpy().astype(np.int64) != ref_acc)
+    assert acc_mism == 0, f"{acc_mism} of {ref_acc.size} int32 accumulators differ"
+    assert np.array_equal(bf16_bits(out2), ref)
     assert case.status() == 0
 
 
@@ -121,12 +130,14 @@ def test_mlp_shapes_on_sampled_columns(N, K):
     M = 128
     x, xs, W, ws = synth.w8a8_inputs(M, K, N, seed=4000 + N, dist="mlp")
     case = W8A8Case(x, xs, W, ws)
-    got = bf16_bits(case.run())
+    out, acc = case.run_acc()
     torch.cuda.synchronize()
+    got = bf16_bits(out)
     rng = np.random.default_rng(N + K)
     cols = np.unique(np.concatenate([rng.choice(N, 96, replace=False), [0, 127, 128, N - 128, N - 1]]))
-    ref = oracle.w8a8_gemm(x, xs, np.ascontiguousarray(W[:, cols]), ws[cols])
-    np.testing.assert_array_equal(got[:, cols], ref)
+    Wc = np.ascontiguousarray(W[:, cols])
+    np.testing.assert_array_equal(got[:, cols], oracle.w8a8_gemm(x, xs, Wc, ws[cols]))
+    np.testing.assert_array_equal(acc.cpu().numpy()[:, cols].astype(np.int64), oracle.w8a8_acc(x, Wc))
     assert case.status() == 0
 
 
