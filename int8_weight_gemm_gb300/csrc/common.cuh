@@ -50,6 +50,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// One non-blocking test of the phase of `parity` (mbarrier.test_wait never waits).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // The same, but a thread whose phase is not complete stays suspended (issuing nothing) until the
 // phase completes or about kSuspendHintNs have passed, instead of returning at once: waiting warps
 // then leave the issue slots to the warps that have work.
@@ -66,10 +77,12 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t pa
 
 // Wait for the phase of `parity` to complete.  Bounded: gives up when another thread of the CTA
 // has raised *abort, or after `limit` cycles (then records the timeout in *status and raises
-// *abort).  Returns true when the phase completed.
+// *abort).  Returns true when the phase completed.  The first look is a non-blocking test; after
+// that the thread stays suspended in the hinted try_wait until the phase completes (measured on
+// GB300: one suspension per blocking wait, resumed about 64 ns after the completing arrival).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint32_t* status, long long limit = kWaitTimeoutCycles) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
     if (mbar_try_wait_suspend(bar, parity)) return true;

@@ -527,24 +527,22 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
           flush(segsum + (segs & 1) * kSegInts);
           since = 0;
         }
-        // Convert every weight fragment first, then issue the MMAs k-step by k-step, so that the
-        // two MMAs into one accumulator are a whole k-step's worth of independent MMAs apart.
-        uint32_t a[kWarpSubTiles][2][4];
+        // Sub-tile by sub-tile: its two k-steps' weight fragments, then its MMAs.  Only one
+        // sub-tile's converted fragments are live at a time (measured fewer instructions and
+        // 0.4 us less on the gate_up-sized call than converting all four first).
 #pragma unroll
         for (int u = 0; u < kWarpSubTiles; ++u) {
-          offset_bytes_to_subnormal_pairs(w[u].x, a[u][0][0], a[u][0][2]);   // row g,   k 8c+0..3
-          offset_bytes_to_subnormal_pairs(w[u].y, a[u][0][1], a[u][0][3]);   // row g+8, k 8c+0..3
-          offset_bytes_to_subnormal_pairs(w[u].z, a[u][1][0], a[u][1][2]);   // row g,   k 8c+4..7
-          offset_bytes_to_subnormal_pairs(w[u].w, a[u][1][1], a[u][1][3]);   // row g+8, k 8c+4..7
-        }
+          uint32_t a[2][4];
+          offset_bytes_to_subnormal_pairs(w[u].x, a[0][0], a[0][2]);   // row g,   k 8c+0..3
+          offset_bytes_to_subnormal_pairs(w[u].y, a[0][1], a[0][3]);   // row g+8, k 8c+0..3
+          offset_bytes_to_subnormal_pairs(w[u].z, a[1][0], a[1][2]);   // row g,   k 8c+4..7
+          offset_bytes_to_subnormal_pairs(w[u].w, a[1][1], a[1][3]);   // row g+8, k 8c+4..7
 #pragma unroll
-        for (int st = 0; st < 2; ++st)
-#pragma unroll
-          for (int u = 0; u < kWarpSubTiles; ++u)
+          for (int st = 0; st < 2; ++st)
 #pragma unroll
             for (int j = 0; j < NT8; ++j)
-              mma_f16_16816(facc[u][j], a[u][st][0], a[u][st][1], a[u][st][2], a[u][st][3], b[j][2 * st],
-                            b[j][2 * st + 1]);
+              mma_f16_16816(facc[u][j], a[st][0], a[st][1], a[st][2], a[st][3], b[j][2 * st], b[j][2 * st + 1]);
+        }
         ++since;
       } else {
         __syncwarp();

@@ -219,7 +219,7 @@ def q8_0_rms_gemv(x_bits: np.ndarray, g_bits: np.ndarray, eps: float, q: np.ndar
     return y, rs
 
 
-def q8_0_rms_bound(x_bits, g_bits, eps, q, d_bits, rel: float = 4e-3) -> np.ndarray:
+def q8_0_rms_bound(x_bits, g_bits, eps, q, d_bits, rel: float = 8e-3) -> np.ndarray:
     """Per-output error bound of the RMS-norm read: rel * rs[t] * ||x_t * g||_2 * ||w_n||_2."""
     x_bits = _c(x_bits, np.uint16)
     g_bits = _c(g_bits, np.uint16)

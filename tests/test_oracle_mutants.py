@@ -142,7 +142,7 @@ def _bound_rows_reversed(x_bits, q, d_bits, rel=2e-3):
     return rel * np.outer(xn[::-1], wn)
 
 
-def _rms_bound_without_rs(x_bits, g_bits, eps, q, d_bits, rel=4e-3):
+def _rms_bound_without_rs(x_bits, g_bits, eps, q, d_bits, rel=8e-3):
     T, K = x_bits.shape
     xg = np.zeros(T, dtype=np.float64)
     oracle.lib().oracle_q8_0_rms_xg_norms(oracle._ptr(np.ascontiguousarray(x_bits, np.uint16)),

@@ -547,5 +547,5 @@ def test_q8_0_rms_bound_scales_with_rs_and_the_norms():
     _, rs = oracle.q8_0_rms_gemv(xb, gb, 1e-6, q, db)
     xg = (x.double() * g.double()).numpy()
     w = d.astype(np.float64).repeat(32, axis=1) * q.astype(np.float64)
-    expect = 4e-3 * rs[:, None] * np.sqrt((xg * xg).sum(axis=1))[:, None] * np.sqrt((w * w).sum(axis=1))[None, :]
+    expect = 8e-3 * rs[:, None] * np.sqrt((xg * xg).sum(axis=1))[:, None] * np.sqrt((w * w).sum(axis=1))[None, :]
     np.testing.assert_allclose(b, expect, rtol=1e-13)

@@ -1,10 +1,10 @@
 """Q8_0 read with an RMS-norm prologue on the GPU against the oracle.
 
 y = rs * (x * g) @ (d * q), rs the inverse RMS of each activation row.  Per output the error bound
-is 4e-3 * rs[t] * ||x_t * g||_2 * ||w_n||_2: the staged product x * g is rounded once to bf16
-(relative 2^-9 per term, at most 2^-9 * ||x_t * g|| ||w_n|| over the sum by Cauchy-Schwarz), the
-output is rounded once to bf16 (2^-9 |y| <= 2^-9 rs ||x_t * g|| ||w_n||), and fp32 summation adds
-far less.  Cases cover the three combine paths of the read (one CTA per tile, a cluster per tile,
+is 8e-3 * rs[t] * ||x_t * g||_2 * ||w_n||_2: the staged product x * g is rounded once to bf16
+(relative 2^-8 per term, bf16 having 8 significant bits: at most 2^-8 * ||x_t * g|| ||w_n|| over the
+sum by Cauchy-Schwarz), the output is rounded once to bf16 (2^-8 |y| <= 2^-8 rs ||x_t * g|| ||w_n||),
+and fp32 summation and rs add far less (2^-7 = 7.8e-3).  Cases cover the three combine paths of the read (one CTA per tile, a cluster per tile,
 split CTAs with the last-arrival combine), ragged N, eps = 0 and large eps, a constant g against
 the plain read, graph replay and programmatic dependent launch.
 """
