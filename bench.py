@@ -493,8 +493,10 @@ def time_tensor_memory_arm(args, dev, hbm_peak):
     shape: the same rotating-weight graph replays as the headline, reported beside it.  At M = 128
     a weight byte feeds 256 flops, so the line gives both the HBM fraction (weight bytes) and the
     tensor fraction (2 M N K flops against the measured bf16 peak; the fp16 kind has the same
-    nominal rate)."""
+    nominal rate).  The arm is forced (W8A8_FLAG_TENSOR_MEMORY_ARM)."""
     import torch
+
+    import int8_weight_gemm_gb300 as lib8
 
     peaks = {}
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -504,7 +506,8 @@ def time_tensor_memory_arm(args, dev, hbm_peak):
     tensor_peak = float(peaks.get("bf16_tflops", 1900.0))
     rows = []
     for (M, K, N, dist, seed) in ((128, 4096, 1536, "uniform", 5128), (128, 4096, 24576, "mlp", 5)):
-        r = time_gemm(M, K, N, dist, seed, min(args.steps, 100), args.warmup, device=dev, want_e2e=False)
+        r = time_gemm(M, K, N, dist, seed, min(args.steps, 100), args.warmup, device=dev, want_e2e=False,
+                      flags=lib8.W8A8_FLAG_TENSOR_MEMORY_ARM)
         r.pop("inputs")
         us = r["us_median"]
         gbs = r["wbytes"] / (us * 1e-6) / 1e9

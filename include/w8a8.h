@@ -24,8 +24,9 @@
  *    nothing and returns a non-zero status; nothing is thrown and nothing is printed.
  *  - w8a8_gemm and q8_0_gemv do no host synchronisation, allocation or memset, so a call can be
  *    captured into a CUDA graph and replayed.  Each is one kernel launch, except w8a8_gemm with
- *    M > 32: two launches (the activations converted to fp16 into the workspace, then the GEMM
- *    as a programmatic dependent of that launch).
+ *    M > 32: two launches on the tcgen05 arm (the activations converted to fp16 into the
+ *    workspace, then the GEMM as a programmatic dependent of that launch), or ceil(M / 32) decode
+ *    launches when the automatic plan runs row chunks (see W8A8_FLAG_TENSOR_MEMORY_ARM).
  *  - A workspace is caller-owned device memory, at least 256-byte aligned, sized with the
  *    *_workspace_bytes queries and zeroed once with w8a8_workspace_init (outside any capture)
  *    before its first use.  Every call leaves it ready for the next one (each arrival counter is
@@ -73,6 +74,12 @@ enum {
      * them, then synchronise once).  Consecutive calls then overlap one call's weight prefetch with
      * the previous call's tail, inside a CUDA graph as well. */
     W8A8_FLAG_PDL = 1u,
+    /* w8a8_gemm with 32 < M <= 128: always run the tcgen05 arm.  Without it the automatic plan
+     * (blocks == 0) runs, whichever a cost model measured on GB300 predicts faster, either that
+     * arm or the decode arm over consecutive chunks of at most 32 activation rows (one launch per
+     * chunk, in stream order on the one workspace); an explicit blocks > 0 selects the tcgen05
+     * arm as well.  Both give the same bits. */
+    W8A8_FLAG_TENSOR_MEMORY_ARM = 2u,
     /* Test hook of the device fault path (w8a8_gemm and its variants only; not for production
      * calls).  One warp of the first CTA waits on a pipeline barrier that nothing completes, with a
      * bound of a few milliseconds instead of the usual second.  The wait runs out, the kernel
@@ -160,8 +167,8 @@ int w8a8_pack_weights(const int8_t* W, int K, int N, void* W_packed, void* ws, s
  *           the SM count, at most one CTA per slab).  Must not exceed the number of slabs.
  *           For M > 32 the same rule applies to T = ceil(N/128) tiles of 128 rows (two packed
  *           tiles each) x KB units of 32 k, with one CTA per SM by default.
- *  flags    0 or W8A8_FLAG_PDL (W8A8_FLAG_TEST_STALL for tests of the fault path); any other bit
- *           is INVALID_ARG.
+ *  flags    0, W8A8_FLAG_PDL and/or W8A8_FLAG_TENSOR_MEMORY_ARM (W8A8_FLAG_TEST_STALL for tests
+ *           of the fault path); any other bit is INVALID_ARG.
  *  ws       workspace of at least w8a8_workspace_bytes(M, K, N, blocks) bytes.
  *  The int32 sums are exact (the result does not depend on `blocks`), and the epilogue order is
  *  fixed, so the output is bit-identical for every `blocks` and every replay.
@@ -199,9 +206,16 @@ typedef struct {
                               arrival count (chosen when both fit; halves the atomics) */
     int tile_rows;         /* weight rows per tile: 64 (M <= 32) or 128 (M > 32) */
     int tensor_memory;     /* 1: the tcgen05 arm (accumulators in tensor memory), 0: decode arm */
+    int row_chunks;        /* decode launches per call: 1, or ceil(M / 32) when the automatic plan
+                              runs 32 < M <= 128 as row chunks (the other fields describe the plan
+                              of a 32-row chunk) */
 } w8a8_plan_t;
 
 int w8a8_plan(int M, int K, int N, int blocks, w8a8_plan_t* plan);
+
+/* The plan of a w8a8_gemm call made with `flags` (W8A8_FLAG_TENSOR_MEMORY_ARM changes the plan of
+ * 32 < M <= 128; the other flags do not).  Host-only. */
+int w8a8_plan_flags(int M, int K, int N, int blocks, unsigned flags, w8a8_plan_t* plan);
 
 /* The slab runs of a plan (the split described at w8a8_gemm's `blocks`): bounds[i] = first
  * slab of CTA i, bounds[blocks] = total slabs (slab u covers tile u / KB, k in

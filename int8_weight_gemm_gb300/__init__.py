@@ -41,6 +41,7 @@ __all__ = [
 
 W8A8_OK = 0
 W8A8_FLAG_PDL = 1
+W8A8_FLAG_TENSOR_MEMORY_ARM = 2
 W8A8_FLAG_TEST_STALL = 0x100
 W8A8_DEV_WAIT_TIMEOUT = 1
 W8A8_DEV_COUNTER_CORRUPT = 2
@@ -66,6 +67,7 @@ class PlanT(ctypes.Structure):
         ("combine_pack_bits", ctypes.c_int),
         ("tile_rows", ctypes.c_int),
         ("tensor_memory", ctypes.c_int),
+        ("row_chunks", ctypes.c_int),
     ]
 
 
@@ -84,6 +86,7 @@ SIGNATURES = {
     "w8a8_gemm_no_alloc": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_i, _c_i, _c_i, _c_i, ctypes.c_uint, _c_p], _c_i),
     "w8a8_gemm_no_alloc_status": ([_c_p, ctypes.POINTER(ctypes.c_uint32)], _c_i),
     "w8a8_plan": ([_c_i, _c_i, _c_i, _c_i, ctypes.POINTER(PlanT)], _c_i),
+    "w8a8_plan_flags": ([_c_i, _c_i, _c_i, _c_i, ctypes.c_uint, ctypes.POINTER(PlanT)], _c_i),
     "w8a8_split_bounds": ([_c_i, _c_i, _c_i, ctypes.POINTER(ctypes.c_longlong), _c_i], _c_i),
     "w8a8_split_bounds_m": ([_c_i, _c_i, _c_i, _c_i, ctypes.POINTER(ctypes.c_longlong), _c_i], _c_i),
     "q8_0_workspace_bytes": ([_c_i, _c_i, _c_i], _c_sz),
@@ -191,9 +194,9 @@ def q8_0_workspace_bytes(T_max: int, K: int, N: int) -> int:
     return int(lib().q8_0_workspace_bytes(T_max, K, N))
 
 
-def w8a8_plan(M: int, K: int, N: int, blocks: int = 0) -> dict:
+def w8a8_plan(M: int, K: int, N: int, blocks: int = 0, flags: int = 0) -> dict:
     p = PlanT()
-    _check("w8a8_plan", lib().w8a8_plan(M, K, N, blocks, ctypes.byref(p)))
+    _check("w8a8_plan_flags", lib().w8a8_plan_flags(M, K, N, blocks, flags, ctypes.byref(p)))
     return {f: getattr(p, f) for f, _ in PlanT._fields_}
 
 

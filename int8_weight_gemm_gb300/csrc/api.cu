@@ -85,15 +85,53 @@ cudaError_t encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType type, voi
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-int any_plan(int M, int K, int N, int blocks, int sm_count, AnyPlan* plan) {
-  plan->tc = M > kDecodeMaxM;
-  return plan->tc ? tc_plan(M, K, N, blocks, sm_count, &plan->t) : gemm_plan(M, K, N, blocks, sm_count, &plan->g);
+// Cost model of the two ways to run 32 < M <= 128, from graph-replay timings on GB300 (cold
+// weights, 152 SMs) of both kernels over five weight shapes from 6 to 96 MiB: each call costs a
+// fixed part plus a part proportional to the packed weight's size, by decode n8-tile count and by
+// the tensor-memory kernel's MMA width.  The decode kernel's per-byte cost grows with M (its MMA
+// and activation-conversion work per weight byte do), the tensor-memory kernel's much less, so
+// row chunks win on small weights and the tensor-memory kernel on large ones.
+static double decode_cost_us(int nt8, double w_mib) {
+  static const double fixed[5] = {0.0, 3.82, 4.62, 5.10, 5.55}, per_mib[5] = {0.0, 0.156, 0.176, 0.270, 0.362};
+  return fixed[nt8] + per_mib[nt8] * w_mib;
+}
+static double tc_cost_us(int M, double w_mib) { return M <= 64 ? 15.05 + 0.474 * w_mib : 24.0 + 0.499 * w_mib; }
+
+int any_plan(int M, int K, int N, int blocks, int sm_count, AnyPlan* plan, bool force_tc) {
+  plan->tc = false;
+  plan->chunks = 1;
+  if (M <= kDecodeMaxM) return gemm_plan(M, K, N, blocks, sm_count, &plan->g);
+  int rc = tc_plan(M, K, N, blocks, sm_count, &plan->t);
+  if (rc != W8A8_OK) return rc;
+  plan->tc = true;
+  if (force_tc || blocks > 0) return W8A8_OK;
+  const int chunks = (M + kDecodeMaxM - 1) / kDecodeMaxM;
+  const int last = M - kDecodeMaxM * (chunks - 1);
+  const double w_mib = (double)((N + 63) / 64) * 64.0 * (double)K / 1048576.0;
+  const double t_chunks = (chunks - 1) * decode_cost_us(4, w_mib) + decode_cost_us((last + 7) / 8, w_mib);
+  if (t_chunks >= tc_cost_us(M, w_mib)) return W8A8_OK;
+  if ((rc = gemm_plan(kDecodeMaxM, K, N, 0, sm_count, &plan->g)) != W8A8_OK) return rc;
+  if ((rc = gemm_plan(last, K, N, 0, sm_count, &plan->g_last)) != W8A8_OK) return rc;
+  plan->tc = false;
+  plan->chunks = chunks;
+  return W8A8_OK;
 }
 
 cudaError_t any_launch(const AnyPlan& pl, const int8_t* x, const float* xs, const void* wp, const float* wsc, void* out,
                        int M, int K, int N, void* ws, bool pdl, cudaStream_t stream, int* acc, bool stall) {
-  return pl.tc ? tc_launch(pl.t, x, xs, wp, wsc, out, M, K, N, ws, pdl, stream, acc, stall)
-               : gemm_launch(pl.g, x, xs, wp, wsc, out, M, K, N, ws, pdl, stream, acc, stall);
+  if (pl.tc) return tc_launch(pl.t, x, xs, wp, wsc, out, M, K, N, ws, pdl, stream, acc, stall);
+  if (pl.chunks == 1) return gemm_launch(pl.g, x, xs, wp, wsc, out, M, K, N, ws, pdl, stream, acc, stall);
+  // Row chunks, one decode launch each, in stream order on the one workspace (each call leaves it
+  // zeroed for the next).  With PDL each chunk's weight prefetch overlaps the previous chunk's tail.
+  for (int c = 0; c < pl.chunks; ++c) {
+    const int m0 = kDecodeMaxM * c;
+    const int rows = c + 1 < pl.chunks ? kDecodeMaxM : M - m0;
+    const GemmPlan& g = c + 1 < pl.chunks ? pl.g : pl.g_last;
+    cudaError_t e = gemm_launch(g, x + (size_t)m0 * K, xs + m0, wp, wsc, static_cast<uint16_t*>(out) + (size_t)m0 * N,
+                                rows, K, N, ws, pdl, stream, acc ? acc + (size_t)m0 * N : nullptr, stall && c == 0);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace w8a8
@@ -151,22 +189,28 @@ size_t w8a8_workspace_bytes(int M_max, int K, int N, int blocks) {
   size_t best = 0;
   // One plan per kernel variant that some M in [1, M_max] runs: the decode arm's n8-tile counts,
   // then the tensor-memory arm's two MMA widths.
+  // For M > 32 the tensor-memory arm's plan is taken whether or not the automatic plan picks it
+  // (the decode arm's row chunks need no more than its M = 32 plan, probed here as well).
   const int probes[] = {1, 9, 17, 25, 32, 33, 64, 65, 128};
   for (int m : probes) {
     if (m > M_max) break;
     AnyPlan pl;
-    if (any_plan(m, K, N, blocks, sms, &pl) != W8A8_OK) return 0;
+    if (any_plan(m, K, N, blocks, sms, &pl, true) != W8A8_OK) return 0;
     if (pl.workspace_bytes() > best) best = pl.workspace_bytes();
   }
   AnyPlan pl;
-  if (any_plan(M_max, K, N, blocks, sms, &pl) != W8A8_OK) return 0;
+  if (any_plan(M_max, K, N, blocks, sms, &pl, true) != W8A8_OK) return 0;
   return pl.workspace_bytes() > best ? pl.workspace_bytes() : best;
 }
 
-int w8a8_plan(int M, int K, int N, int blocks, w8a8_plan_t* plan) {
+int w8a8_plan(int M, int K, int N, int blocks, w8a8_plan_t* plan) { return w8a8_plan_flags(M, K, N, blocks, 0u, plan); }
+
+int w8a8_plan_flags(int M, int K, int N, int blocks, unsigned flags, w8a8_plan_t* plan) {
   if (!plan) return W8A8_ERR_INVALID_ARG;
+  if (flags & ~(unsigned)(W8A8_FLAG_PDL | W8A8_FLAG_TENSOR_MEMORY_ARM | W8A8_FLAG_TEST_STALL))
+    return W8A8_ERR_INVALID_ARG;
   AnyPlan ap;
-  int rc = any_plan(M, K, N, blocks, device_sm_count(), &ap);
+  int rc = any_plan(M, K, N, blocks, device_sm_count(), &ap, (flags & W8A8_FLAG_TENSOR_MEMORY_ARM) != 0);
   if (rc != W8A8_OK) return rc;
   if (ap.tc) {
     const TcPlan& pl = ap.t;
@@ -183,6 +227,7 @@ int w8a8_plan(int M, int K, int N, int blocks, w8a8_plan_t* plan) {
     plan->combine_pack_bits = 0;
     plan->tile_rows = 128;
     plan->tensor_memory = 1;
+    plan->row_chunks = 1;
     return W8A8_OK;
   }
   const GemmPlan& pl = ap.g;
@@ -199,6 +244,7 @@ int w8a8_plan(int M, int K, int N, int blocks, w8a8_plan_t* plan) {
   plan->combine_pack_bits = pl.pack_f;
   plan->tile_rows = 64;
   plan->tensor_memory = 0;
+  plan->row_chunks = ap.chunks;
   return W8A8_OK;
 }
 
@@ -244,9 +290,10 @@ static int gemm_call(const char* name, const int8_t* x_q, const float* x_scale, 
                      const float* w_scale, void* out, int32_t* acc, int M, int K, int N, int blocks, unsigned flags,
                      void* ws, size_t ws_bytes, void* stream) {
   if (!x_q || !x_scale || !W_packed || !w_scale || !out || !ws) return W8A8_ERR_INVALID_ARG;
-  if (flags & ~(unsigned)(W8A8_FLAG_PDL | W8A8_FLAG_TEST_STALL)) return W8A8_ERR_INVALID_ARG;
+  if (flags & ~(unsigned)(W8A8_FLAG_PDL | W8A8_FLAG_TENSOR_MEMORY_ARM | W8A8_FLAG_TEST_STALL))
+    return W8A8_ERR_INVALID_ARG;
   AnyPlan pl;
-  int rc = any_plan(M, K, N, blocks, device_sm_count(), &pl);
+  int rc = any_plan(M, K, N, blocks, device_sm_count(), &pl, (flags & W8A8_FLAG_TENSOR_MEMORY_ARM) != 0);
   if (rc != W8A8_OK) return rc;
   if (!aligned(x_q, 16) || !aligned(W_packed, 16) || !aligned(out, 16) || !aligned(x_scale, 4) ||
       !aligned(w_scale, 4) || !aligned(ws, 256) || !aligned(acc, 4))

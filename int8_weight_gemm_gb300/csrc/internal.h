@@ -52,15 +52,23 @@ cudaError_t tc_launch(const TcPlan& pl, const int8_t* x, const float* xs, const 
                       int M, int K, int N, void* ws, bool pdl, cudaStream_t stream, int* acc = nullptr,
                       bool stall = false);
 
-// Either arm, chosen by M.
+// Either arm.  M <= 32: the decode kernel.  M > 32: the tensor-memory kernel, or the decode kernel
+// over consecutive row chunks of at most 32 (chunks > 1), whichever the measured cost model of
+// any_plan predicts faster; an explicit CTA count (blocks > 0) or force_tc selects the
+// tensor-memory kernel.
 struct AnyPlan {
   bool tc;
-  GemmPlan g;
+  int chunks;      // decode launches: 1, or ceil(M / 32) row chunks for M > 32
+  GemmPlan g;      // decode plan (of the 32-row chunks when chunks > 1)
+  GemmPlan g_last; // chunks > 1: the plan of the last chunk's M - 32 (chunks - 1) rows
   TcPlan t;
-  size_t workspace_bytes() const { return tc ? t.workspace_bytes : g.workspace_bytes; }
+  size_t workspace_bytes() const {
+    if (tc) return t.workspace_bytes;
+    return chunks > 1 && g_last.workspace_bytes > g.workspace_bytes ? g_last.workspace_bytes : g.workspace_bytes;
+  }
 };
 
-int any_plan(int M, int K, int N, int blocks, int sm_count, AnyPlan* plan);
+int any_plan(int M, int K, int N, int blocks, int sm_count, AnyPlan* plan, bool force_tc = false);
 cudaError_t any_launch(const AnyPlan& pl, const int8_t* x, const float* xs, const void* wp, const float* wsc, void* out,
                        int M, int K, int N, void* ws, bool pdl, cudaStream_t stream, int* acc = nullptr,
                        bool stall = false);

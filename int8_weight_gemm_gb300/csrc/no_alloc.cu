@@ -104,10 +104,11 @@ extern "C" int w8a8_gemm_no_alloc(const int8_t* x_q, const float* x_scale, const
                                   const float* w_scale, void* out, int M, int K, int N, int blocks,
                                   unsigned flags, void* stream) {
   if (!x_q || !x_scale || !W_packed || !w_scale || !out) return W8A8_ERR_INVALID_ARG;
-  if (flags & ~(unsigned)(W8A8_FLAG_PDL | W8A8_FLAG_TEST_STALL)) return W8A8_ERR_INVALID_ARG;
+  if (flags & ~(unsigned)(W8A8_FLAG_PDL | W8A8_FLAG_TENSOR_MEMORY_ARM | W8A8_FLAG_TEST_STALL))
+    return W8A8_ERR_INVALID_ARG;
   const int sms = device_sm_count();
   AnyPlan pl;
-  const int rc = any_plan(M, K, N, blocks, sms, &pl);
+  const int rc = any_plan(M, K, N, blocks, sms, &pl, (flags & W8A8_FLAG_TENSOR_MEMORY_ARM) != 0);
   if (rc != W8A8_OK) return rc;
   auto misaligned = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; };
   if (misaligned(x_q, 16) || misaligned(W_packed, 16) || misaligned(out, 16) || misaligned(x_scale, 4) ||

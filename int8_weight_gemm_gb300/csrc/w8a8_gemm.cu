@@ -436,8 +436,11 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
   const int slab = warp & (kStageSlabs - 1);
   const int half = warp / kStageSlabs;
   const int sub0 = kHalfSubTiles ? kWarpSubTiles * half : 0;   // first sub-tile of this warp
-  // The activation sums: warps of one slab position share its activations, so one of them adds.
-  const bool sums_x = !kHalfSubTiles || half == 0;
+  // The activation sums.  NT8 <= 2: each warp sums the rows of every n8 tile of its slabs.
+  // NT8 >= 3: the two warps of a slab position see the same activations, so each sums half of
+  // the n8 tiles (j in [xj0, xj0 + kXsumTiles)), which also halves the registers it needs.
+  constexpr int kXsumTiles = kHalfSubTiles ? (NT8 + 1) / 2 : NT8;
+  const int xj0 = kHalfSubTiles ? half * kXsumTiles : 0;
   float facc[kWarpSubTiles][NT8][4];
 #pragma unroll
   for (int u = 0; u < kWarpSubTiles; ++u)
@@ -445,9 +448,9 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
     for (int j = 0; j < NT8; ++j)
 #pragma unroll
       for (int r = 0; r < 4; ++r) facc[u][j][r] = 0.f;
-  int xsum[NT8];          // sum of this lane's activation bytes of row 8j + g over the segment
+  int xsum[kXsumTiles];   // sum of this lane's activation bytes of row 8 (xj0 + i) + g over the segment
 #pragma unroll
-  for (int j = 0; j < NT8; ++j) xsum[j] = 0;
+  for (int i = 0; i < kXsumTiles; ++i) xsum[i] = 0;
   int since = 0;          // slabs accumulated in fp32 by this warp since its last flush
   int segs = 0;
   int q = 0;              // CTA-wide stage index of the current segment's first stage
@@ -519,7 +522,13 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
           const uint2 v = *reinterpret_cast<const uint2*>(xr + j * 1024);
           offset_bytes_to_half2(v.x ^ 0x80808080u, b[j][0], b[j][1]);
           offset_bytes_to_half2(v.y ^ 0x80808080u, b[j][2], b[j][3]);
-          if (sums_x) xsum[j] = __dp4a((int)v.y, 0x01010101, __dp4a((int)v.x, 0x01010101, xsum[j]));
+          if (!kHalfSubTiles) {
+            xsum[j] = __dp4a((int)v.y, 0x01010101, __dp4a((int)v.x, 0x01010101, xsum[j]));
+          } else {
+#pragma unroll
+            for (int i = 0; i < kXsumTiles; ++i)
+              if (j == xj0 + i) xsum[i] = __dp4a((int)v.y, 0x01010101, __dp4a((int)v.x, 0x01010101, xsum[i]));
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[slot]);   // registers hold everything this warp needs
@@ -563,16 +572,14 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
     int* const sums = segsum + buf * kSegInts;
     if (since) flush(sums);
     since = 0;
-    if (sums_x) {
-      // Row 8j + g's activation sum over this warp's slabs: the four lanes of a row hold 32 k each.
+    // Row 8j + g's activation sum over this warp's slabs: the four lanes of a row hold 32 k each.
 #pragma unroll
-      for (int j = 0; j < NT8; ++j) {
-        int sx = xsum[j];
-        sx += __shfl_xor_sync(0xffffffffu, sx, 1);
-        sx += __shfl_xor_sync(0xffffffffu, sx, 2);
-        if (c == 0) atomicAdd(&xsum_sm[buf][8 * j + g], sx);
-        xsum[j] = 0;
-      }
+    for (int i = 0; i < kXsumTiles; ++i) {
+      int sx = xsum[i];
+      sx += __shfl_xor_sync(0xffffffffu, sx, 1);
+      sx += __shfl_xor_sync(0xffffffffu, sx, 2);
+      if (c == 0 && xj0 + i < NT8) atomicAdd(&xsum_sm[buf][8 * (xj0 + i) + g], sx);
+      xsum[i] = 0;
     }
     ++segs;
     if (kMulti && seg_end != b1) {

@@ -10,7 +10,10 @@ def bf16_bits(t: torch.Tensor) -> np.ndarray:
 
 
 class W8A8Case:
-    """Device copies of one W8A8 problem (packed weight, scales, workspace)."""
+    """Device copies of one W8A8 problem (packed weight, scales, workspace).  base_flags are OR-ed
+    into every call's flags."""
+
+    base_flags = 0
 
     def __init__(self, x_q, x_scale, W, w_scale, M_max=None, blocks=0):
         dev = torch.device("cuda")
@@ -26,12 +29,12 @@ class W8A8Case:
 
     def run(self, out=None, blocks=None, flags=0):
         return lib8.w8a8_gemm(self.x, self.xs, self.Wp, self.ws_scale, self.ws, self.N, out=out,
-                              blocks=self.blocks if blocks is None else blocks, flags=flags)
+                              blocks=self.blocks if blocks is None else blocks, flags=flags | self.base_flags)
 
     def run_acc(self, blocks=None, flags=0):
         """The same call through w8a8_gemm_acc: (out bf16, acc int32) as device tensors."""
         return lib8.w8a8_gemm_acc(self.x, self.xs, self.Wp, self.ws_scale, self.ws, self.N,
-                                  blocks=self.blocks if blocks is None else blocks, flags=flags)
+                                  blocks=self.blocks if blocks is None else blocks, flags=flags | self.base_flags)
 
     def status(self):
         return lib8.w8a8_workspace_status(self.ws)

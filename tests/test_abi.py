@@ -128,11 +128,11 @@ def test_plan_shape_and_limits():
 
 def test_tensor_memory_arm_plan():
     # 32 < M <= 128: 128-row tiles (two packed tiles), one CTA per SM, MMA N = 64 or 128.
-    p = lib8.w8a8_plan(128, 4096, 1536)
+    p = lib8.w8a8_plan(128, 4096, 1536, flags=lib8.W8A8_FLAG_TENSOR_MEMORY_ARM)
     assert p["tensor_memory"] == 1 and p["tile_rows"] == 128 and p["n8_tiles"] == 16
     assert p["n_tiles"] == 12 and p["k_blocks"] == 128 and p["slabs"] == 12 * 128
     assert p["blocks"] == 152 and p["threads"] == 608 and p["smem_bytes"] <= 227 * 1024
-    q = lib8.w8a8_plan(33, 4096, 320)
+    q = lib8.w8a8_plan(33, 4096, 320, flags=lib8.W8A8_FLAG_TENSOR_MEMORY_ARM)
     assert q["n8_tiles"] == 8 and q["n_tiles"] == 3 and q["threads"] == 640
     assert lib8.w8a8_plan(32, 4096, 320)["tensor_memory"] == 0
     # header, counters (one per tile, padded to 256 bytes), int32 planes [tile][128][128] whatever
@@ -142,16 +142,38 @@ def test_tensor_memory_arm_plan():
     # with at least as many 128-row tiles as SMs, a CTA count dividing the tile count (whole tiles)
     assert lib8.w8a8_plan(128, 4096, 24576)["blocks"] == 96
     assert lib8.w8a8_plan(128, 12288, 4096)["blocks"] == 152
-    # the size query for M_max covers both arms
+    # the size query for M_max covers both arms, forced or automatic, and the row-chunk plans
     big = lib8.w8a8_workspace_bytes(128, 4096, 1536)
-    assert all(lib8.w8a8_plan(M, 4096, 1536)["workspace_bytes"] <= big for M in range(1, 129))
+    for f in (0, lib8.W8A8_FLAG_TENSOR_MEMORY_ARM):
+        assert all(lib8.w8a8_plan(M, 4096, 1536, flags=f)["workspace_bytes"] <= big for M in range(1, 129))
     assert lib8.w8a8_workspace_bytes(129, 4096, 1536) == 0
+
+
+def test_automatic_plan_routes_mid_m_by_the_cost_model():
+    # 32 < M <= 128: decode row chunks on small weights, the tensor-memory arm on large ones; the
+    # flag or an explicit CTA count forces the tensor-memory arm.
+    p = lib8.w8a8_plan(64, 4096, 2560)
+    assert p["tensor_memory"] == 0 and p["row_chunks"] == 2 and p["n8_tiles"] == 4
+    assert lib8.w8a8_plan(96, 4096, 1536)["row_chunks"] == 3
+    assert lib8.w8a8_plan(40, 4096, 1536)["row_chunks"] == 2
+    g = lib8.w8a8_plan(128, 4096, 24576)
+    assert g["tensor_memory"] == 1 and g["row_chunks"] == 1
+    assert lib8.w8a8_plan(64, 4096, 2560, flags=lib8.W8A8_FLAG_TENSOR_MEMORY_ARM)["tensor_memory"] == 1
+    assert lib8.w8a8_plan(64, 4096, 2560, blocks=40)["tensor_memory"] == 1
+    assert all(lib8.w8a8_plan(M, 4096, 1536)["row_chunks"] == 1 for M in range(1, 33))
+    # every M in (32, 128] at these shapes is either arm, and the size query covers both
+    for (K, N) in ((4096, 1536), (2048, 4096), (4096, 24576)):
+        big = lib8.w8a8_workspace_bytes(128, K, N)
+        for M in range(33, 129):
+            p = lib8.w8a8_plan(M, K, N)
+            assert p["workspace_bytes"] <= big
+            assert p["tensor_memory"] == 1 or p["row_chunks"] == -(-M // 32)
 
 
 @pytest.mark.parametrize("M,K,N,blocks", [(64, 4096, 1536, 0), (128, 4096, 24576, 0), (100, 2048, 384, 7),
                                           (33, 4000, 320, 0), (128, 32, 8, 1), (65, 12288, 4096, 304)])
 def test_tensor_memory_arm_split_bounds(M, K, N, blocks):
-    plan = lib8.w8a8_plan(M, K, N, blocks)
+    plan = lib8.w8a8_plan(M, K, N, blocks, flags=lib8.W8A8_FLAG_TENSOR_MEMORY_ARM)
     G, U, KB, T = plan["blocks"], plan["slabs"], plan["k_blocks"], plan["n_tiles"]
     assert T == -(-N // 128) and U == T * KB
     b = np.array(lib8.w8a8_split_bounds(K, N, G, M=M))
@@ -318,7 +340,7 @@ def test_misaligned_and_short_workspace_are_rejected_on_the_host():
     assert L.w8a8_gemm(odd, a, a, a, a, 16, 4096, 1536, 0, 0, a, ws_need, None) == 3
     assert L.w8a8_gemm(a, a, odd, a, a, 16, 4096, 1536, 0, 0, a, ws_need, None) == 3
     assert L.w8a8_gemm(a, a, a, a, a, 16, 4096, 1536, 0, 0, a, ws_need - 1, None) == 4
-    assert L.w8a8_gemm(a, a, a, a, a, 16, 4096, 1536, 0, 2, a, ws_need, None) == 1      # unknown flag
+    assert L.w8a8_gemm(a, a, a, a, a, 16, 4096, 1536, 0, 4, a, ws_need, None) == 1      # unknown flag
     qws = lib8.q8_0_workspace_bytes(6, 4096, 320)
     assert L.q8_0_gemv(odd, a, a, a, 6, 4096, 320, 0, a, qws, None) == 3
     assert L.q8_0_gemv(a, a, a, a, 6, 4096, 320, 0, a, qws - 1, None) == 4

@@ -222,7 +222,7 @@ def _run_cta(b0, b1, KB, n_mma, seed, fault=None):
                                           (100, 2048, 384, 7), (33, 4000, 320, 0), (128, 512, 1024, 3),
                                           (64, 96, 136, 0), (128, 4096, 1536, 1)])
 def test_protocol_has_no_aliasing_and_no_deadlock(M, K, N, blocks):
-    plan = lib8.w8a8_plan(M, K, N, blocks)
+    plan = lib8.w8a8_plan(M, K, N, blocks, flags=lib8.W8A8_FLAG_TENSOR_MEMORY_ARM)
     assert plan["tensor_memory"] == 1
     G, KB = plan["blocks"], plan["k_blocks"]
     bounds = lib8.w8a8_split_bounds(K, N, G, M=M)

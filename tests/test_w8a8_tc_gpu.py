@@ -17,6 +17,13 @@ import oracle
 import synth
 from gpu_util import W8A8Case, bf16_bits
 
+
+class TcCase(W8A8Case):
+    """A W8A8 case whose calls always run the tensor-memory arm (the automatic plan may run 32-row
+    decode chunks instead on small weights; those are tested in test_w8a8_route_gpu.py)."""
+
+    base_flags = lib8.W8A8_FLAG_TENSOR_MEMORY_ARM
+
 pytestmark = pytest.mark.gpu
 
 
@@ -48,7 +55,7 @@ def _check(case, x, xs, W, ws, blocks=None):
 
 def test_plan_uses_the_tensor_memory_arm():
     for M, n8 in ((33, 8), (64, 8), (65, 16), (128, 16)):
-        pl = lib8.w8a8_plan(M, 4096, 1536)
+        pl = lib8.w8a8_plan(M, 4096, 1536, flags=lib8.W8A8_FLAG_TENSOR_MEMORY_ARM)
         assert pl["tensor_memory"] == 1 and pl["tile_rows"] == 128 and pl["n8_tiles"] == n8
     assert lib8.w8a8_plan(32, 4096, 1536)["tensor_memory"] == 0
 
@@ -56,7 +63,7 @@ def test_plan_uses_the_tensor_memory_arm():
 @pytest.mark.parametrize("M", [33, 40, 48, 63, 64, 65, 96, 127, 128])
 def test_ragged_m(M):
     x, xs, W, ws = synth.w8a8_inputs(M, 1024, 200, seed=M)
-    case = W8A8Case(x, xs, W, ws)
+    case = TcCase(x, xs, W, ws)
     _check(case, x, xs, W, ws)
 
 
@@ -66,7 +73,7 @@ def test_ragged_shapes(M, K, N):
     # N = 320: five packed tiles, so the third 128-row tile has only its first half; K = 4000 and
     # K = 416: the last stage of a segment holds fewer than four 32-k units.
     x, xs, W, ws = synth.w8a8_inputs(M, K, N, seed=K + N + M)
-    case = W8A8Case(x, xs, W, ws)
+    case = TcCase(x, xs, W, ws)
     _check(case, x, xs, W, ws)
 
 
@@ -75,7 +82,7 @@ def test_every_split_count_is_bit_identical(blocks):
     # 3 tiles of 128 rows x 64 units: one CTA per tile up to one CTA per unit.
     M, K, N = 100, 2048, 384
     x, xs, W, ws = synth.w8a8_inputs(M, K, N, seed=3)
-    case = W8A8Case(x, xs, W, ws, blocks=blocks)
+    case = TcCase(x, xs, W, ws, blocks=blocks)
     _check(case, x, xs, W, ws)
 
 
@@ -99,7 +106,7 @@ def test_adversarial_cancelling_partial_sums(M):
     acc = oracle.w8a8_acc(x, W)
     assert np.abs(acc).max() <= 256 and np.abs(acc).max() > 0
     for blocks in (0, 1, 37):
-        case = W8A8Case(x, xs, W, ws, blocks=blocks)
+        case = TcCase(x, xs, W, ws, blocks=blocks)
         _check(case, x, xs, W, ws)
 
 
@@ -110,7 +117,7 @@ def test_extremes(fill):
     W = np.full((K, N), fill, np.int8)
     xs = np.full(M, 2.0**-10, np.float32)
     ws = np.full(N, 2.0**-12, np.float32)
-    case = W8A8Case(x, xs, W, ws)
+    case = TcCase(x, xs, W, ws)
     _check(case, x, xs, W, ws)
 
 
@@ -118,7 +125,7 @@ def test_extremes(fill):
 @pytest.mark.parametrize("N,K", [(1536, 4096), (2560, 4096), (4096, 2048)])
 def test_sweep_shapes(M, N, K):
     x, xs, W, ws = synth.w8a8_inputs(M, K, N, seed=1000 * 3 + M)
-    case = W8A8Case(x, xs, W, ws)
+    case = TcCase(x, xs, W, ws)
     _check(case, x, xs, W, ws)
 
 
@@ -129,7 +136,7 @@ def test_mlp_shapes_on_sampled_columns(N, K):
     # them) and those are compared bit for bit.
     M = 128
     x, xs, W, ws = synth.w8a8_inputs(M, K, N, seed=4000 + N, dist="mlp")
-    case = W8A8Case(x, xs, W, ws)
+    case = TcCase(x, xs, W, ws)
     out, acc = case.run_acc()
     torch.cuda.synchronize()
     got = bf16_bits(out)
@@ -144,7 +151,7 @@ def test_mlp_shapes_on_sampled_columns(N, K):
 def test_untouched_rows_and_columns():
     M, K, N = 70, 512, 200
     x, xs, W, ws = synth.w8a8_inputs(M, K, N, seed=5)
-    case = W8A8Case(x, xs, W, ws)
+    case = TcCase(x, xs, W, ws)
     buf = torch.full((M * N + 64,), 3.0, dtype=torch.bfloat16, device="cuda")
     res = case.run(out=buf[: M * N].view(M, N))
     torch.cuda.synchronize()
@@ -155,7 +162,7 @@ def test_untouched_rows_and_columns():
 def test_counters_and_planes_return_to_zero_and_calls_repeat():
     M, K, N = 128, 4096, 1536
     x, xs, W, ws = synth.w8a8_inputs(M, K, N, seed=2)
-    case = W8A8Case(x, xs, W, ws, blocks=1536)      # workspace sized for the largest split count
+    case = TcCase(x, xs, W, ws, blocks=1536)      # workspace sized for the largest split count
     ref = oracle.w8a8_gemm(x, xs, W, ws)
     for blocks in (0, 1, 152, 1536, 5, 0):
         got = bf16_bits(case.run(blocks=blocks))
@@ -175,7 +182,8 @@ def test_decode_and_tensor_memory_arms_share_one_workspace():
     wsd = torch.from_numpy(ws).cuda()
     for M in (16, 128, 32, 33, 1, 64, 128, 40, 128, 8):
         x, xs, _, _ = synth.w8a8_inputs(M, K, N, seed=40 + M)
-        out = lib8.w8a8_gemm(torch.from_numpy(x).cuda(), torch.from_numpy(xs).cuda(), Wp, wsd, work, N)
+        out = lib8.w8a8_gemm(torch.from_numpy(x).cuda(), torch.from_numpy(xs).cuda(), Wp, wsd, work, N,
+                             flags=lib8.W8A8_FLAG_TENSOR_MEMORY_ARM if M > 32 else 0)
         torch.cuda.synchronize()
         np.testing.assert_array_equal(bf16_bits(out), oracle.w8a8_gemm(x, xs, W, ws))
     assert (work[4:_zeroed_end(N)] == 0).all()
@@ -185,7 +193,7 @@ def test_decode_and_tensor_memory_arms_share_one_workspace():
 def test_graph_replay_is_bitwise_the_direct_call():
     M, K, N = 96, 4096, 1536
     x, xs, W, ws = synth.w8a8_inputs(M, K, N, seed=8)
-    case = W8A8Case(x, xs, W, ws)
+    case = TcCase(x, xs, W, ws)
     direct = bf16_bits(case.run())
     out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     s = torch.cuda.Stream()
@@ -209,7 +217,7 @@ def test_graph_replay_is_bitwise_the_direct_call():
 def test_pdl_calls_back_to_back_are_bit_identical(blocks):
     M, K, N = 128, 4096, 1536
     x, xs, W, ws = synth.w8a8_inputs(M, K, N, seed=21)
-    case = W8A8Case(x, xs, W, ws, blocks=blocks)
+    case = TcCase(x, xs, W, ws, blocks=blocks)
     torch.cuda.synchronize()
     ref = oracle.w8a8_gemm(x, xs, W, ws)
     outs = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(6)]
