@@ -413,6 +413,35 @@ def time_read_ceiling(dev, nbytes=1 << 30, reps=20):
             "kernel": "w8a8_read_probe (16-byte loads, 2 x SMs x 512 threads)"}
 
 
+def time_mma_rates(dev, iters=4096, reps=5):
+    """The library's tensor-pipe rate probe: the fp16 m16n8k16 MMA the decode kernel uses against
+    the int8 m16n8k32 MMA it does not, each as 2 x SMs CTAs of 8 warps (four per sub-partition),
+    timed with CUDA events."""
+    import torch
+
+    import int8_weight_gemm_gb300 as lib8
+
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sink = torch.zeros(1, dtype=torch.int64, device=dev)
+    out = []
+    for kind, form, per_mma in ((0, "mma.sync m16n8k16 f16 x f16 -> f32", 4096), (1, "mma.sync m16n8k32 s8 x s8 -> s32", 8192)):
+        for _ in range(2):
+            lib8.w8a8_mma_rate_probe(kind, iters, sink)
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            lib8.w8a8_mma_rate_probe(kind, iters, sink)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        s = e0.elapsed_time(e1) / 1e3
+        ops = 2 * sms * 8 * iters * 8 * per_mma * reps
+        out.append({"form": form, "kind": kind, "tera_ops_per_s": round(ops / s / 1e12, 1),
+                    "us_per_launch": round(s * 1e6 / reps, 2), "mmas_per_launch": 2 * sms * 8 * iters * 8})
+    return out
+
+
 def time_graph_calls(make_call, R, calls=256, reps=20):
     """Median us per call of a CUDA graph of `calls` launches cycling over R buffer sets;
     make_call(i) issues call i on the current stream."""
@@ -686,6 +715,7 @@ def run_ours(args):
                             for f in (0, lib8.W8A8_FLAG_PDL)]
         out["tensor_memory_arm"] = time_tensor_memory_arm(args, dev, peak)
         out["read_ceiling"] = time_read_ceiling(dev)
+        out["mma_rates"] = time_mma_rates(dev)
         if not args.no_q8:
             out["quantisation"] = time_quantisation_rows(peak)
         out["roofline"]["frac_of_read_ceiling"] = round(achieved / out["read_ceiling"]["value"], 4)
@@ -783,20 +813,50 @@ def run_sweep(args):
             print(json.dumps(row), flush=True)
             del r
             torch.cuda.empty_cache()
+    if args.no_q8:
+        return
     for (K8, N8) in ((4096, 320), (320, 4096)):
         for T in (1, 4, 6):
             for flags in flags_list:
                 print(json.dumps(time_q8(T, K8, N8, flags=flags)), flush=True)
                 print(json.dumps(time_q8(T, K8, N8, flags=flags, rms=True)), flush=True)
+    for r in time_mma_rates(torch.device("cuda")):
+        print(json.dumps(r), flush=True)
 
 
 def run_ncu_driver(args):
     """Profiling driver (for ncu captures, not a bench line): the default workload's public-API
-    calls, eagerly, on rotating packed weights (each call reads a different weight copy), then exit."""
+    calls, eagerly, on rotating packed weights (each call reads a different weight copy), then exit.
+    --ncu-op q8_0 runs the Q8_0 read instead (--ncu-shape T,K,N), --ncu-op mma the tensor-pipe rate
+    probe (both kinds)."""
     import torch
 
     import int8_weight_gemm_gb300 as lib8
     import synth
+
+    if args.ncu_op == "mma":
+        sink = torch.zeros(1, dtype=torch.int64, device="cuda")
+        for _ in range(args.ncu_driver):
+            for kind in (0, 1):
+                lib8.w8a8_mma_rate_probe(kind, 256, sink)
+        torch.cuda.synchronize()
+        print(json.dumps({"ncu_driver_calls": args.ncu_driver, "op": "mma"}))
+        return
+    if args.ncu_op == "q8_0":
+        T, K, N = (int(v) for v in (args.ncu_shape or "6,4096,320").split(","))
+        x, q, d = synth.q8_0_inputs(T, K, N, seed=7)
+        xd = x.cuda()
+        qs = [torch.from_numpy(q).cuda() for _ in range(8)]
+        ds = [torch.from_numpy(d.view(np.int16)).cuda() for _ in range(8)]
+        qws = lib8.alloc_workspace(lib8.q8_0_workspace_bytes(T, K, N))
+        for i in range(args.ncu_driver):
+            lib8.q8_0_gemv(xd, qs[i % 8], ds[i % 8], qws)
+        torch.cuda.synchronize()
+        status = lib8.w8a8_workspace_status(qws)
+        print(json.dumps({"ncu_driver_calls": args.ncu_driver, "op": "q8_0", "device_status": status}))
+        if status != 0:
+            sys.exit(1)
+        return
 
     cfg = DEFAULT
     M, K, N = cfg["M"], cfg["K"], cfg["N"]
@@ -831,6 +891,7 @@ def build_parser():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-q8", action="store_true", help="skip the Q8_0 timings")
     ap.add_argument("--ncu-shape", default="", help="M,K,N for --ncu-driver (default: the headline shape)")
+    ap.add_argument("--ncu-op", default="w8a8", choices=["w8a8", "q8_0", "mma"], help="what --ncu-driver calls")
     ap.add_argument("--ncu-driver", type=int, default=0,
                     help="profiling driver: this many eager calls of the default workload, then exit")
     return ap

@@ -331,6 +331,16 @@ int q8_0_blocks_from_split(const int8_t* q, const void* d, void* blocks, int K, 
  * aligned.  Errors: INVALID_ARG, MISALIGNED, CUDA. */
 int w8a8_read_probe(const void* buf, size_t bytes, void* sink, void* stream);
 
+/* Measurement helper (not part of either operator): the tensor-pipe rate of the two register-fed
+ * MMA forms an int8 product can take, for the caller to time.  kind 0: mma.sync m16n8k16 with fp16
+ * operands and fp32 accumulation (4096 flops per MMA; the form the decode kernel uses, after its
+ * exact int8 -> fp16 conversion); kind 1: mma.sync m16n8k32 with int8 operands and int32
+ * accumulation (8192 int ops per MMA).  One launch of 2 x SM-count CTAs of 256 threads; every warp
+ * issues iters x 8 independent MMAs, so one call performs 2 x SMs x 8 x iters x 8 MMAs.  sink: an
+ * 8-byte aligned device word written only in a case real runs practically never produce.
+ * iters in [1, 2^24].  Errors: INVALID_ARG, MISALIGNED, CUDA. */
+int w8a8_mma_rate_probe(int kind, int iters, void* sink, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

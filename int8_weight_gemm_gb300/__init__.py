@@ -91,6 +91,7 @@ SIGNATURES = {
     "w8a8_split_bounds_m": ([_c_i, _c_i, _c_i, _c_i, ctypes.POINTER(ctypes.c_longlong), _c_i], _c_i),
     "q8_0_workspace_bytes": ([_c_i, _c_i, _c_i], _c_sz),
     "w8a8_read_probe": ([_c_p, _c_sz, _c_p, _c_p], _c_i),
+    "w8a8_mma_rate_probe": ([_c_i, _c_i, _c_p, _c_p], _c_i),
     "w8a8_quantize_activations": ([_c_p, _c_p, _c_p, _c_i, _c_i, _c_p], _c_i),
     "q8_0_quantize": ([_c_p, _c_p, _c_p, _c_i, _c_i, _c_p], _c_i),
     "q8_0_split_from_blocks": ([_c_p, _c_p, _c_p, _c_i, _c_i, _c_p], _c_i),
@@ -348,6 +349,14 @@ def w8a8_read_probe(buf, sink, stream=None) -> None:
     _dev(sink, "sink", 8)
     _on_cuda(buf=buf, sink=sink)
     _check("w8a8_read_probe", lib().w8a8_read_probe(_ptr(buf), _nbytes(buf), _ptr(sink), _stream(stream)))
+
+
+def w8a8_mma_rate_probe(kind: int, iters: int, sink, stream=None) -> None:
+    """Launch the tensor-pipe rate probe (kind 0: fp16 m16n8k16, kind 1: int8 m16n8k32); the
+    caller times it.  `sink` is an 8-byte device tensor the kernel may write."""
+    _dev(sink, "sink", 8)
+    _on_cuda(sink=sink)
+    _check("w8a8_mma_rate_probe", lib().w8a8_mma_rate_probe(kind, iters, _ptr(sink), _stream(stream)))
 
 
 def w8a8_quantize_activations(x, x_q=None, x_scale=None, stream=None):

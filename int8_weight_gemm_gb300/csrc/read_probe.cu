@@ -44,3 +44,63 @@ extern "C" int w8a8_read_probe(const void* buf, size_t bytes, void* sink, void* 
   if (e != cudaSuccess) return record_cuda_error(e, "w8a8_read_probe");
   return W8A8_OK;
 }
+
+// ---------------------------------------------------------------------------------------------
+// Tensor-pipe rate probe: the two register-fed MMA forms the decode kernel could use for its int8
+// products, timed by the caller.  Each warp runs `iters` rounds of eight independent MMAs (eight
+// accumulator sets, so the pipe never waits on a result) on operands that change every round; the
+// accumulators are folded into a value written only in a case real runs never produce.
+//  kind 0: mma.sync m16n8k16 f16 x f16 -> f32 (the form the decode kernel uses, after converting
+//          int8 to fp16 exactly): 2 * 16 * 8 * 16 = 4096 flops per MMA.
+//  kind 1: mma.sync m16n8k32 s8 x s8 -> s32: 2 * 16 * 8 * 32 = 8192 int ops per MMA.
+// ---------------------------------------------------------------------------------------------
+namespace w8a8 {
+
+template <int KIND>
+__global__ void __launch_bounds__(256) mma_rate_kernel(int iters, unsigned long long* sink) {
+  const uint32_t lane = threadIdx.x & 31;
+  uint32_t a0 = 0x3C003C00u ^ lane, a1 = 0x3C013C01u ^ lane, a2 = 0x3C023C02u, a3 = 0x3C033C03u;
+  uint32_t b0 = 0x3C003C00u ^ (lane << 1), b1 = 0x3C043C04u;
+  float f[8][4] = {};
+  int s[8][4] = {};
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      if (KIND == 0) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(f[r][0]), "+f"(f[r][1]), "+f"(f[r][2]), "+f"(f[r][3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+      } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+            : "+r"(s[r][0]), "+r"(s[r][1]), "+r"(s[r][2]), "+r"(s[r][3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+      }
+    }
+    a0 += 0x00010001u;
+    b1 ^= (uint32_t)it;
+  }
+  uint32_t acc = 0;
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc ^= __float_as_uint(f[r][c]) ^ (uint32_t)s[r][c];
+  if (acc == 0x9E3779B9u) atomicAdd(sink, 1ull);
+}
+
+}  // namespace w8a8
+
+extern "C" int w8a8_mma_rate_probe(int kind, int iters, void* sink, void* stream) {
+  if ((kind != 0 && kind != 1) || iters < 1 || iters > (1 << 24) || !sink) return W8A8_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(sink) & 7u) return W8A8_ERR_MISALIGNED;
+  const int sms = device_sm_count();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned long long* k = static_cast<unsigned long long*>(sink);
+  // Two CTAs of eight warps per SM: four warps per sub-partition, as many as the decode kernel runs.
+  if (kind == 0) mma_rate_kernel<0><<<2 * sms, 256, 0, s>>>(iters, k);
+  else mma_rate_kernel<1><<<2 * sms, 256, 0, s>>>(iters, k);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return record_cuda_error(e, "w8a8_mma_rate_probe");
+  return W8A8_OK;
+}

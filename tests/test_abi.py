@@ -290,6 +290,15 @@ def test_read_probe_checks_its_arguments_on_the_host():
     assert L.w8a8_read_probe(a, 1 << 20, ctypes.c_void_p((1 << 20) + 4), None) == 3
 
 
+def test_mma_rate_probe_checks_its_arguments_on_the_host():
+    L = lib8.lib()
+    a = ctypes.c_void_p(1 << 20)
+    assert L.w8a8_mma_rate_probe(2, 10, a, None) == 1          # unknown kind
+    assert L.w8a8_mma_rate_probe(0, 0, a, None) == 1           # no iterations
+    assert L.w8a8_mma_rate_probe(1, 10, None, None) == 1       # no sink
+    assert L.w8a8_mma_rate_probe(0, 10, ctypes.c_void_p((1 << 20) + 4), None) == 3
+
+
 def test_quantisation_entry_points_check_arguments_on_the_host():
     L = lib8.lib()
     a = ctypes.c_void_p(1 << 20)
