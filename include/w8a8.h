@@ -163,7 +163,8 @@ int w8a8_pack_weights(const int8_t* W, int K, int N, void* W_packed, void* ws, s
  *           is cut into c + 1 (the first blocks % T tiles) or c = blocks / T contiguous parts of
  *           equal length to within one slab, one per CTA, so no CTA spans two tiles; with
  *           blocks < T the tiles are laid end to end and CTA i takes a contiguous run of
- *           ceil or floor(T KB / blocks) slabs (the longer runs first).  0 = automatic (twice
+ *           ceil or floor(T KB / (u blocks)) units of u slabs (the longer runs first), u being
+ *           the plan's split_unit (1 or 4; see w8a8_plan_t).  0 = automatic (twice
  *           the SM count, at most one CTA per slab).  Must not exceed the number of slabs.
  *           For M > 32 the same rule applies to T = ceil(N/128) tiles of 128 rows (two packed
  *           tiles each) x KB units of 32 k, with one CTA per SM by default.
@@ -209,6 +210,10 @@ typedef struct {
     int row_chunks;        /* decode launches per call: 1, or ceil(M / 32) when the automatic plan
                               runs 32 < M <= 128 as row chunks (the other fields describe the plan
                               of a 32-row chunk) */
+    int split_unit;        /* slabs per unit of a run split with blocks < n_tiles: 1, or 4 for the
+                              decode arm when K % 128 == 0 and runs of whole 4-slab units make the
+                              longest run at most 3 % longer (every run then starts on an 8 KiB
+                              boundary of the packed weight) */
 } w8a8_plan_t;
 
 int w8a8_plan(int M, int K, int N, int blocks, w8a8_plan_t* plan);

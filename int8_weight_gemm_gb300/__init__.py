@@ -68,6 +68,7 @@ class PlanT(ctypes.Structure):
         ("tile_rows", ctypes.c_int),
         ("tensor_memory", ctypes.c_int),
         ("row_chunks", ctypes.c_int),
+        ("split_unit", ctypes.c_int),
     ]
 
 

@@ -228,6 +228,7 @@ int w8a8_plan_flags(int M, int K, int N, int blocks, unsigned flags, w8a8_plan_t
     plan->tile_rows = 128;
     plan->tensor_memory = 1;
     plan->row_chunks = 1;
+    plan->split_unit = 1;
     return W8A8_OK;
   }
   const GemmPlan& pl = ap.g;
@@ -245,6 +246,7 @@ int w8a8_plan_flags(int M, int K, int N, int blocks, unsigned flags, w8a8_plan_t
   plan->tile_rows = 64;
   plan->tensor_memory = 0;
   plan->row_chunks = ap.chunks;
+  plan->split_unit = pl.split_unit;
   return W8A8_OK;
 }
 
@@ -257,7 +259,7 @@ int w8a8_split_bounds_m(int M, int K, int N, int blocks, long long* bounds, int 
   const int kb = ap.tc ? ap.t.kb : ap.g.kb;
   const int g = ap.tc ? ap.t.blocks : ap.g.blocks;
   if (n_bounds != g + 1) return W8A8_ERR_INVALID_ARG;
-  const GemmSplit sp = make_gemm_split(n_tiles, kb, g);
+  const GemmSplit sp = make_gemm_split(n_tiles, kb, g, !ap.tc);
   for (int i = 0; i < g; ++i) {
     int b0, b1;
     gemm_split_run(sp, i, &b0, &b1);

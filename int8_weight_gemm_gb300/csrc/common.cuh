@@ -217,17 +217,23 @@ __host__ __device__ __forceinline__ int even_lo(int i, int U, int G) {
 //    c for the rest (c = G / T, e = G % T), part j of P_t taking slabs [even_lo(j), even_lo(j+1))
 //    of the tile's KB.  No CTA crosses a tile, so each CTA finishes exactly one tile segment and
 //    P_t CTAs meet in the tile's combine.
-//  - Linear (G < T): the tiles are laid end to end and CTA i takes a contiguous run of a + 1
-//    (i < r) or a slabs (a = U / G, r = U % G), which may span several tiles.
+//  - Linear (G < T): the tiles are laid end to end and cut into units of 2^qs slabs; CTA i takes
+//    a contiguous run of a + 1 (i < r) or a units (a = U' / G, r = U' % G over the U' = U / 2^qs
+//    units), which may span several tiles.
 // Both cover every slab exactly once with no empty run (G <= U).
 struct GemmSplit {
   int T, KB, G;
   int aligned;
   int c, e;   // tile-aligned: parts per tile, tiles with one extra part
-  int a, r;   // linear: run length, runs one slab longer
+  int a, r;   // linear: run length in units, runs one unit longer
+  int qs;     // linear: log2 of the slabs per unit (0 or 2)
 };
 
-inline GemmSplit make_gemm_split(int T, int KB, int G) {
+// coarse: the decode kernel's split, whose linear runs go in units of 4 slabs (so every run starts
+// on an 8 KiB boundary of the packed weight) when K is a multiple of 128 and the longest run grows
+// by at most 3 %.  Measured on GB300 at K = 4096, N = 24576 (96 MiB of weight, 304 CTAs):
+// 0.5-1.2 us less per call for M = 1..32 than runs cut at any slab.
+inline GemmSplit make_gemm_split(int T, int KB, int G, bool coarse = false) {
   GemmSplit s{};
   s.T = T;
   s.KB = KB;
@@ -236,8 +242,13 @@ inline GemmSplit make_gemm_split(int T, int KB, int G) {
   s.c = G / T;
   s.e = G % T;
   const int U = T * KB;
-  s.a = U / G;
-  s.r = U % G;
+  s.qs = 0;
+  if (!s.aligned && coarse && KB % 4 == 0 && U / 4 >= G) {
+    const long long run1 = (U + G - 1) / G, run4 = 4ll * ((U / 4 + G - 1) / G);
+    if (run4 * 100 <= run1 * 103) s.qs = 2;
+  }
+  s.a = (U >> s.qs) / G;
+  s.r = (U >> s.qs) % G;
   return s;
 }
 
@@ -259,14 +270,15 @@ __host__ __device__ __forceinline__ void gemm_split_run(const GemmSplit& s, int 
     *b0 = t * s.KB + even_lo(j, s.KB, P);
     *b1 = t * s.KB + even_lo(j + 1, s.KB, P);
   } else {
-    *b0 = i * s.a + (i < s.r ? i : s.r);
-    *b1 = *b0 + s.a + (i < s.r ? 1 : 0);
+    *b0 = (i * s.a + (i < s.r ? i : s.r)) << s.qs;
+    *b1 = *b0 + ((s.a + (i < s.r ? 1 : 0)) << s.qs);
   }
 }
 
 // The CTA whose run contains slab u (linear split).
 __host__ __device__ __forceinline__ int gemm_split_owner_linear(const GemmSplit& s, int u) {
-  const int head = s.r * (s.a + 1);   // slabs of the longer runs
+  u >>= s.qs;                         // its unit
+  const int head = s.r * (s.a + 1);   // units of the longer runs
   return u < head ? (int)((unsigned)u / (unsigned)(s.a + 1)) : s.r + (int)((unsigned)(u - head) / (unsigned)s.a);
 }
 

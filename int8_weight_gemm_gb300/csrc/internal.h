@@ -22,6 +22,7 @@ struct GemmPlan {
   long long slabs;
   int blocks, threads, stage_slabs, stages;
   int pack_f;   // split-tile combine: bits per element field of a two-element word (0: one per word)
+  int split_unit;   // slabs per unit of a linear run split (1 or 4)
   size_t smem_bytes, workspace_bytes, partials_offset;
 };
 

@@ -16,12 +16,14 @@
 //  * The weight stream goes HBM -> shared memory through the TMA engine (cp.async.bulk, 1-D,
 //    evict-first L2 policy) into an NS-deep ring of stages, issued by one producer warp.
 //  * int8 tensor-core throughput on this part is far below what a weight stream at HBM speed
-//    needs at M = 16 (measured: mma.sync s8 ~150 TOPS vs fp16 ~600 TFLOPS), so the int8 values
-//    are converted exactly to fp16 (every int8 is an fp16 integer) and multiplied on the fp16
-//    tensor path with fp32 accumulation.  Products are integers of magnitude <= 2^14 and a
-//    partial sum over at most 256 k stays <= 2^22, so every fp32 accumulator value is an exact
-//    integer; the fp32 partials are converted to int32 (exactly) at least every 256 k and summed
-//    in int32.  The result is the int32 sum an int8 MMA would produce, bit for bit.
+//    needs at M = 16 (measured with w8a8_mma_rate_probe: mma.sync s8 158 TOPS against fp16
+//    587 TFLOPS), so the products run on the fp16 tensor path with fp32 accumulation: each
+//    activation int8 becomes the fp16 integer it is, and each weight byte, stored offset binary
+//    (w + 128), becomes the fp16 subnormal (w + 128) * 2^-24 with one byte permute (see
+//    offset_bytes_to_subnormal_pairs).  Every fp32 partial over a window of at most 512 k is then
+//    an exact multiple of 2^-24 below 1; windows are converted to int32 exactly and summed in
+//    int32, and 128 * sum_k x comes off once per tile segment.  The result is the int32 sum an
+//    int8 MMA would produce, bit for bit.
 //  * Weight rows are the MMA's M dimension (16 rows per warp) and the activation rows are its
 //    N dimension (n8 tiles), so M <= 8 wastes nothing on a 16-row MMA tile.
 #include <cuda.h>
@@ -121,26 +123,63 @@ struct GemmParams {
   int debug_stall;    // test hook: one warp of CTA 0 waits on a barrier that nothing completes
 };
 
-// Walks a CTA's run of slabs [b0, b1) as stages of at most SS slabs that never cross a tile.
+// A CTA's run of slabs [b0, b1) is cut by the tile boundaries into segments (one tile's part
+// each).  Every segment but the last is finished by the combine warp (a round trip of returning
+// atomics for a split tile) while the consumer warps stream on, so the segment walked last should
+// be long enough to cover that work.  With tiles of at least 128 k-blocks (K >= 4096) the walk
+// puts the longer of two segments last, and walks three as first, last, then the whole tile in
+// the middle: measured on GB300 0.5 us less per call than the natural order at K = 4096,
+// N = 24576, M = 16 (1.2 us together with the 4-slab run unit of make_gemm_split, 2.7 us at
+// M = 32), and less at K = 8192 as well.  Shorter tiles keep the natural order: moving a whole
+// tile last there made the second sum buffer wait for the first segment's combine behind a short
+// segment (0.5-0.9 us slower at K = 2048 and K = 1024).
 // Slab indices fit in 32 bits (at most 2^14 tiles x 2^11 k-blocks).
+// multi = false: the launch's split gives every CTA a single segment (the tile-aligned split), a
+// compile-time fact that leaves nothing to order.
+struct RunOrder {
+  int b0, b1, KB, t0, nseg, last;   // last: the segment (natural index) walked last
+  __device__ RunOrder(int b0_, int b1_, int KB_, bool multi) : b0(b0_), b1(b1_), KB(KB_) {
+    t0 = b0 / KB;
+    if (!multi) {
+      nseg = 1;
+      last = 0;
+      return;
+    }
+    nseg = b1 > b0 ? (b1 - 1) / KB - t0 + 1 : 0;
+    last = nseg - 1;
+    if (KB >= 128 && nseg == 2 && (t0 + 1) * KB - b0 > b1 - (t0 + 1) * KB) last = 0;
+    if (KB >= 128 && nseg == 3) last = 1;
+  }
+  // Segment (in natural order) walked k-th.
+  __device__ int index(int k) const { return k == nseg - 1 ? last : (k < last ? k : k + 1); }
+  __device__ int begin(int i) const { return max(b0, (t0 + i) * KB); }
+  __device__ int end(int i) const { return min(b1, (t0 + i + 1) * KB); }
+};
+
+// Walks the run as stages of at most SS slabs that never cross a tile, segment by segment in the
+// order of RunOrder.
 struct StageIter {
-  int u, b1, seg_begin, seg_end, t;
-  int KB, ns, ss;
-  __device__ StageIter(int b0_, int b1_, int KB_, int ss_) : u(b0_), b1(b1_), KB(KB_), ss(ss_) { begin_segment(); }
+  RunOrder ro;
+  int k, u, seg_end, t, ns, ss;
+  __device__ StageIter(int b0_, int b1_, int KB_, int ss_, bool multi) : ro(b0_, b1_, KB_, multi), k(0), ss(ss_) {
+    if (ro.nseg > 0) begin_segment();
+  }
   __device__ void begin_segment() {
-    t = u / KB;
-    seg_begin = u;
-    seg_end = min(b1, (t + 1) * KB);
+    const int i = ro.index(k);
+    t = ro.t0 + i;
+    u = ro.begin(i);
+    seg_end = ro.end(i);
     ns = min(ss, seg_end - u);
   }
-  __device__ bool done() const { return u >= b1; }
-  __device__ int kb0() const { return u - t * KB; }
-  __device__ bool last_of_segment() const { return u + ns >= seg_end; }
+  __device__ bool done() const { return k >= ro.nseg; }
+  __device__ int kb0() const { return u - t * ro.KB; }
   __device__ void next() {
     u += ns;
-    if (u >= b1) return;
-    if (u >= seg_end) begin_segment();
-    else ns = min(ss, seg_end - u);
+    if (u < seg_end) {
+      ns = min(ss, seg_end - u);
+    } else if (++k < ro.nseg) {
+      begin_segment();
+    }
   }
 };
 
@@ -208,6 +247,8 @@ __device__ __forceinline__ void store_out(const GemmParams& p, int m, int n, int
 constexpr int kProducerWarp = kConsumerWarps;        // warp 8: lane 0 issues every copy
 constexpr int kProducerThread = 32 * kProducerWarp;
 constexpr int kCombineWarp = kConsumerWarps + 1;     // warp 9: finishes every segment but a CTA's last
+// Returning atomics the combine warp keeps in flight per lane (16 measured no faster).
+constexpr int kCombineBatch = 8;
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
 
 template <int NT8, int NS, bool kMulti>
@@ -253,7 +294,7 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
   // meanwhile clear the segment sums.  Every copy of a stage lands on the stage's full barrier,
   // which counts the weight and activation bytes together.
   const uint32_t xbox = (uint32_t)L::kXRawStage;
-  StageIter it(b0, b1, p.KB, kStageSlabs);   // producer: the next stage to issue
+  StageIter it(b0, b1, p.KB, kStageSlabs, kMulti);   // producer: the next stage to issue
   int pq = 0;                                 // producer: stages issued so far
   uint64_t policy = 0;
   if (threadIdx.x == kProducerThread) {
@@ -305,7 +346,7 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
     if (threadIdx.x != kProducerThread) return;
     pdl_wait();
     if (p.pdl) {
-      StageIter pre(b0, b1, p.KB, kStageSlabs);
+      StageIter pre(b0, b1, p.KB, kStageSlabs, kMulti);
       for (int j = 0; j < pq; pre.next(), ++j)
         tma_load_2d(xraw + j * L::kXRawStage, &p.xmap, pre.kb0() * kKBlock, 0, &full_bar[j]);
     }
@@ -338,27 +379,27 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
     // hands the buffer back.  The consumer warps stream on meanwhile; the last segment, after
     // which there is nothing left to stream, they finish themselves.
     pdl_wait();   // out and the workspace words may belong to the previous call
-    int s = 0;
-    for (int seg_begin = b0, seg_end = 0; seg_begin < b1; seg_begin = seg_end, ++s) {
-      const int t = seg_begin / p.KB;
-      seg_end = min(b1, (t + 1) * p.KB);
-      if (seg_end == b1) break;
+    const RunOrder ro(b0, b1, p.KB, kMulti);
+    for (int s = 0; s + 1 < ro.nseg; ++s) {
+      const int si = ro.index(s);
+      const int t = ro.t0 + si;
+      const int seg_begin = ro.begin(si);
       const int buf = s & 1;
       if (!mbar_wait(&seg_full[buf], (uint32_t)((s >> 1) & 1), &abort_flag, p.status)) return;
       int* const sums = segsum + buf * kSegInts;
       unsigned long long* const tacc = p.tile_acc + (size_t)t * kSegInts;
       const uint32_t n = (uint32_t)gemm_split_contributors(p.split, t);
-      if (seg_begin == t * p.KB) {   // the whole tile is ours (it ends before b1, so it is complete)
+      if (seg_begin == t * p.KB && ro.end(si) == (t + 1) * p.KB) {   // the whole tile is ours
         for (int e = lane; e < kSegInts; e += 32) {
           store_elem(e, t, buf, segment_total(e, buf, sums[e]));
           sums[e] = 0;
         }
       } else if (p.pack_f) {
         constexpr int kHalf = kSegInts / 2, kWords = kHalf / 32;   // words of this lane: lane + 32 w
-        for (int w0 = 0; w0 < kWords; w0 += 8) {
-          unsigned long long old[8];
+        for (int w0 = 0; w0 < kWords; w0 += kCombineBatch) {
+          unsigned long long old[kCombineBatch];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
+          for (int k = 0; k < kCombineBatch; ++k) {
             const int i = lane + 32 * (w0 + k);
             if (w0 + k < kWords)
               old[k] = atom_add_relaxed_u64(tacc + i, pair_increment(segment_total(i, buf, sums[i]),
@@ -366,7 +407,7 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
                                                                      p.pack_f));
           }
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
+          for (int k = 0; k < kCombineBatch; ++k) {
             const int i = lane + 32 * (w0 + k);
             if (w0 + k >= kWords) break;
             long long a, bb;
@@ -384,15 +425,15 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
         }
       } else {
         constexpr int kElems = kSegInts / 32;
-        for (int w0 = 0; w0 < kElems; w0 += 8) {
-          unsigned long long old[8];
+        for (int w0 = 0; w0 < kElems; w0 += kCombineBatch) {
+          unsigned long long old[kCombineBatch];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
+          for (int k = 0; k < kCombineBatch; ++k) {
             const int e = lane + 32 * (w0 + k);
             if (w0 + k < kElems) old[k] = atom_add_relaxed_u64(tacc + e, single_increment(segment_total(e, buf, sums[e])));
           }
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
+          for (int k = 0; k < kCombineBatch; ++k) {
             const int e = lane + 32 * (w0 + k);
             if (w0 + k >= kElems) break;
             const uint32_t arrived = (uint32_t)(old[k] >> 52);
@@ -484,16 +525,19 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
   const int x_off = g * 128 + (((2 * slab + (c >> 1)) ^ g) << 4) + 8 * (c & 1);
   constexpr int kStep = kHalfSubTiles ? 1 : 2;   // stages from one of this warp's stages to the next
 
-  // The run [b0, b1) is walked segment by segment (one tile's part each); a segment of n slabs is
-  // ceil(n / 4) stages of the CTA-wide stage sequence, the last one possibly partial.  q is the
+  // The run [b0, b1) is walked segment by segment (one tile's part each, in RunOrder's order); a
+  // segment of n slabs is ceil(n / 4) stages of the CTA-wide stage sequence, the last one possibly
+  // partial.  q is the
   // CTA-wide index of the segment's first stage; this warp visits only its own stages nq, whose
   // ring slot and phase parity it keeps up to date as it goes.
   int nq = kHalfSubTiles ? 0 : half;   // next CTA-wide stage this warp visits (< NS here)
   int slot = nq;
   uint32_t phase = 0;
-  for (int seg_begin = b0, seg_end = 0; seg_begin < b1; seg_begin = seg_end) {
-    const int t = seg_begin / p.KB;
-    seg_end = min(b1, (t + 1) * p.KB);
+  const RunOrder ro(b0, b1, p.KB, kMulti);
+  for (int k = 0; k < ro.nseg; ++k) {
+    const int si = ro.index(k);
+    const int t = ro.t0 + si;
+    const int seg_begin = ro.begin(si), seg_end = ro.end(si);
     const int seg_slabs = seg_end - seg_begin;
     const int seg_stages = (seg_slabs + kStageSlabs - 1) / kStageSlabs;
     // Start of a segment: count the tile's contributors and fetch its w_scale now, off the
@@ -582,7 +626,7 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
       xsum[i] = 0;
     }
     ++segs;
-    if (kMulti && seg_end != b1) {
+    if (kMulti && k + 1 < ro.nseg) {
       // An earlier segment: hand it to the combine warp and stream on.
       __syncwarp();
       if (lane == 0) mbar_arrive(&seg_full[buf]);
@@ -696,7 +740,7 @@ int gemm_plan(int M, int K, int N, int blocks, int sm_count, GemmPlan* plan) {
     int bits = 0;
     while ((1ll << bits) <= lim) ++bits;
     const int f = bits + 1, count_bits = 64 - 2 * f;
-    const GemmSplit sp = make_gemm_split(pl.n_tiles, pl.kb, pl.blocks);
+    const GemmSplit sp = make_gemm_split(pl.n_tiles, pl.kb, pl.blocks, true);
     int most = 0;
     for (int t = 0; t < pl.n_tiles; ++t) {
       const int c = gemm_split_contributors(sp, t);
@@ -705,6 +749,7 @@ int gemm_plan(int M, int K, int N, int blocks, int sm_count, GemmPlan* plan) {
     pl.pack_f = (count_bits >= 1 && count_bits < 63 && (long long)most < (1ll << count_bits)) ? f : 0;
   }
   pl.threads = pl.blocks >= pl.n_tiles ? kThreadsNoCombine : kThreads;
+  pl.split_unit = 1 << make_gemm_split(pl.n_tiles, pl.kb, pl.blocks, true).qs;
   pl.stage_slabs = kStageSlabs;
   pl.stages = gemm_stages(pl.nt8);
   pl.smem_bytes = gemm_smem_bytes(pl.nt8);
@@ -758,7 +803,7 @@ cudaError_t gemm_launch(const GemmPlan& pl, const int8_t* x, const float* xs, co
   p.K = K;
   p.N = N;
   p.KB = pl.kb;
-  p.split = make_gemm_split(pl.n_tiles, pl.kb, pl.blocks);
+  p.split = make_gemm_split(pl.n_tiles, pl.kb, pl.blocks, true);
   p.pack_f = pl.pack_f;
   p.pdl = pdl ? 1 : 0;
   p.acc_out = acc;

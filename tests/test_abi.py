@@ -74,15 +74,39 @@ def test_split_bounds_cover_every_slab_once(K, N, blocks):
             part = sizes[cs[0]:cs[-1] + 1]
             assert part.max() - part.min() <= 1
     else:
-        # Linear: runs of a + 1 slabs, then runs of a; the kernel counts a tile's contributors
-        # from the owners of its first and last slab with this arithmetic.
-        a, r = U // G, U % G
-        assert (sizes[:r] == a + 1).all() and (sizes[r:] == a).all()
+        # Linear: runs of a + 1 units of q slabs, then runs of a; the kernel counts a tile's
+        # contributors from the owners of its first and last slab with this arithmetic.
+        q = plan["split_unit"]
+        assert q in (1, 4) and U % q == 0
+        a, r = (U // q) // G, (U // q) % G
+        assert (sizes[:r] == q * (a + 1)).all() and (sizes[r:] == q * a).all()
         def owner_of(u):
+            u //= q
             head = r * (a + 1)
             return u // (a + 1) if u < head else r + (u - head) // a
         for t, cs in enumerate(contrib):
             assert owner_of(t * KB + KB - 1) - owner_of(t * KB) + 1 == len(cs)
+
+
+@pytest.mark.parametrize("K,N,blocks,unit", [
+    (4096, 24576, 0, 4),    # 49152 slabs over 304 CTAs: runs of 164 / 160 against 162 / 161 slabs
+    (4096, 24576, 304, 4),
+    (4096, 1536, 0, 1),     # tile-aligned split: units do not apply
+    (96, 24576, 0, 1),      # K / 32 = 3 k-blocks: no 4-slab unit inside a tile
+    (128, 25600, 0, 1),     # 1600 slabs: whole units would make the longest run 8 against 6 slabs
+    (8192, 32768, 0, 4),
+    (4096, 24576, 7, 4),
+])
+def test_linear_split_unit_follows_its_rule(K, N, blocks, unit):
+    plan = lib8.w8a8_plan(16, K, N, blocks)
+    assert plan["split_unit"] == unit
+    b = np.array(lib8.w8a8_split_bounds(K, N, plan["blocks"]))
+    if unit == 4:
+        assert (b % 4 == 0).all()   # every run starts on an 8 KiB boundary of the packed weight
+        U, G = plan["slabs"], plan["blocks"]
+        assert np.diff(b).max() * 100 <= -(-U // G) * 103
+    # The tensor-memory arm keeps runs of single 32-k units.
+    assert lib8.w8a8_plan(64, K, N, 0, flags=lib8.W8A8_FLAG_TENSOR_MEMORY_ARM)["split_unit"] == 1
 
 
 def test_automatic_split_keeps_every_cta_inside_one_tile_for_small_outputs():

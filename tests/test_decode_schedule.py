@@ -25,13 +25,19 @@ STAGE_SLABS = 4
 
 
 def _segments(b0, b1, KB):
-    """(tile, first slab, end slab) of each segment of the run [b0, b1)."""
+    """(tile, first slab, end slab) of each segment of the run [b0, b1), in the order the kernel
+    walks them: with tiles of at least 128 k-blocks two segments swap when the first is the
+    longer and three go first, last, middle; otherwise the natural order."""
     out, u = [], b0
     while u < b1:
         t = u // KB
         end = min(b1, (t + 1) * KB)
         out.append((t, u, end))
         u = end
+    if KB >= 128 and len(out) == 2 and out[0][2] - out[0][1] > out[1][2] - out[1][1]:
+        out = [out[1], out[0]]
+    elif len(out) == 3 and KB >= 128:
+        out = [out[0], out[2], out[1]]
     return out
 
 
@@ -159,6 +165,7 @@ def test_planted_protocol_fault_is_caught(fault, half_subtiles):
 @pytest.mark.parametrize("NS", [6, 8, 10])
 @pytest.mark.parametrize("half_subtiles", [False, True])
 def test_decode_protocol_on_long_runs_with_several_segments(NS, half_subtiles):
-    for (b0, b1, KB) in [(0, 300, 128), (5, 263, 128), (100, 140, 7), (3, 4, 128), (0, 129, 64)]:
+    for (b0, b1, KB) in [(0, 300, 128), (5, 263, 128), (100, 140, 7), (3, 4, 128), (0, 129, 64),
+                         (30, 200, 128), (100, 200, 128), (10, 150, 64)]:
         for seed in range(3):
             _run_cta(b0, b1, KB, NS, half_subtiles, multi=True, seed=seed + b1)
