@@ -272,16 +272,20 @@ def test_read_probe_runs_and_leaves_its_input_alone():
     assert torch.equal(buf, ref)
 
 
-@pytest.mark.parametrize("K,N,blocks", [(65536, 256, 3), (65536, 256, 1), (4096, 256, 3)])
+@pytest.mark.parametrize("K,N,blocks", [(65536, 256, 3), (65536, 256, 1), (4096, 256, 3), (4096, 512, 3),
+                                        (2048, 512, 3), (4096, 1536, 10)])
 def test_multi_segment_ctas_with_both_word_formats(K, N, blocks):
     # Fewer CTAs than tiles: each CTA streams a run across several tiles, and the combine warp
     # finishes every segment but a CTA's last.  K = 65536 leaves no room for two elements per word
-    # (one-element words); K = 4096 uses two-element words.
+    # (one-element words); the others use two-element words.  The runs go in 4-slab units, and the
+    # walk orders of a CTA's segments all occur: two swapped (K = 65536 and 4096 with N = 256),
+    # three as first, last, middle (K = 4096, N = 512 and 1536), three or more in natural order
+    # (K = 2048, and the runs of four segments).
     M = 5
     x, xs, W, ws = synth.w8a8_inputs(M, K, N, seed=K + blocks)
     plan = lib8.w8a8_plan(M, K, N, blocks)
-    assert plan["threads"] == 320
-    assert plan["combine_pack_bits"] == (0 if K == 65536 else 28)
+    assert plan["threads"] == 320 and plan["split_unit"] == 4
+    assert plan["combine_pack_bits"] == (0 if K == 65536 else {4096: 28, 2048: 27}[K])
     case = W8A8Case(x, xs, W, ws, blocks=blocks)
     _check(case, x, xs, W, ws)
     torch.cuda.synchronize()
