@@ -85,17 +85,22 @@ cudaError_t encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType type, voi
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Cost model of the two ways to run 32 < M <= 128, from graph-replay timings on GB300 (cold
-// weights, 152 SMs) of both kernels over five weight shapes from 6 to 96 MiB: each call costs a
-// fixed part plus a part proportional to the packed weight's size, by decode n8-tile count and by
-// the tensor-memory kernel's MMA width.  The decode kernel's per-byte cost grows with M (its MMA
-// and activation-conversion work per weight byte do), the tensor-memory kernel's much less, so
-// row chunks win on small weights and the tensor-memory kernel on large ones.
+// Cost model of the two ways to run 32 < M <= 128: least-squares lines through graph-replay
+// timings on GB300 (cold weights, 152 SMs) of both kernels over six weight shapes from 6 to 96 MiB
+// (K x N = 4096 x 1536, 4096 x 2560, 2048 x 4096, 4096 x 8192, 12288 x 4096, 4096 x 24576), the
+// decode kernel at M = 8, 16, 24, 32 and the tensor-memory kernel at M = 48 ... 128: each call
+// costs a fixed part plus a part proportional to the packed weight's size, by decode n8-tile count
+// and by the tensor-memory kernel's MMA width.  The decode kernel's per-byte cost grows with M (its
+// MMA and activation-conversion work per weight byte do), the tensor-memory kernel's much less, so
+// row chunks win on small weights and the tensor-memory kernel on large ones.  The decode lines fit
+// within 7 %; the tensor-memory kernel's times depend on how its tiles fall over the SMs and fit
+// only within 22 %, so the choice can miss near the crossover (by at most 7 us on the measured
+// shapes, against 20 us for the lines this model replaced).
 static double decode_cost_us(int nt8, double w_mib) {
-  static const double fixed[5] = {0.0, 3.82, 4.62, 5.10, 5.55}, per_mib[5] = {0.0, 0.156, 0.176, 0.270, 0.362};
+  static const double fixed[5] = {0.0, 3.97, 4.77, 4.31, 4.67}, per_mib[5] = {0.0, 0.150, 0.164, 0.298, 0.333};
   return fixed[nt8] + per_mib[nt8] * w_mib;
 }
-static double tc_cost_us(int M, double w_mib) { return M <= 64 ? 15.05 + 0.474 * w_mib : 24.0 + 0.499 * w_mib; }
+static double tc_cost_us(int M, double w_mib) { return M <= 64 ? 17.79 + 0.451 * w_mib : 29.87 + 0.459 * w_mib; }
 
 int any_plan(int M, int K, int N, int blocks, int sm_count, AnyPlan* plan, bool force_tc) {
   plan->tc = false;
