@@ -355,7 +355,10 @@ def time_gemm(M, K, N, dist, seed, steps, warmup, blocks=0, device=None, sample_
 def time_e2e(lib8, M, K, N, xd, xsd, packs, wsd, wsp, blocks, dev, steps, flags=0):
     """The same call through the public API with host buffers: every step copies that step's
     activations and their scales from pinned host memory (one contiguous staging buffer, so one
-    copy), runs the GEMM on a cold weight, and reads the result back to pinned host memory."""
+    copy), runs the GEMM on a cold weight, and reads the result back to pinned host memory.  The
+    steps are captured in a CUDA graph (copy in, GEMM, copy out, per step), as a serving engine
+    captures its decode step; the same steps issued eagerly from Python, bound by the host's launch
+    rate, are reported beside it."""
     import torch
 
     R = len(packs)
@@ -371,21 +374,50 @@ def time_e2e(lib8, M, K, N, xd, xsd, packs, wsd, wsp, blocks, dev, steps, flags=
     outh = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
     out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream(dev)
+
+    def step(i):
+        stage_d.copy_(stage_h, non_blocking=True)
+        lib8.w8a8_gemm(x_dev, xs_dev, packs[i % R], wsd, wsp, N, out=out, blocks=blocks, flags=flags, stream=stream)
+        outh.copy_(out, non_blocking=True)
+
+    # Eager: one Python-issued step after another.
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         for i in range(steps + 3):
             if i == 3:
                 e0.record(stream)
-            stage_d.copy_(stage_h, non_blocking=True)
-            lib8.w8a8_gemm(x_dev, xs_dev, packs[i % R], wsd, wsp, N, out=out, blocks=blocks, flags=flags, stream=stream)
-            outh.copy_(out, non_blocking=True)
+            step(i)
         e1.record(stream)
     stream.synchronize()
-    per_step_us = e0.elapsed_time(e1) * 1e3 / steps
+    eager_us = e0.elapsed_time(e1) * 1e3 / steps
+    # Graph: C steps per replay, cycling over the rotating weights.
+    C = R * max(1, math.ceil(32 / R))
+    with torch.cuda.stream(stream):
+        for i in range(C):
+            step(i)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(C):
+            step(i)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    reps = max(3, steps // C)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    per_step_us = e0.elapsed_time(e1) * 1e3 / (reps * C)
+    del g
     wbytes = lib8.w8a8_packed_weight_bytes(K, N)
     return {"value": wbytes / per_step_us / 1e3, "unit": "GB/s", "us_per_step": per_step_us,
-            "h2d_bytes_per_step": nb, "d2h_bytes_per_step": 2 * M * N}
+            "h2d_bytes_per_step": nb, "d2h_bytes_per_step": 2 * M * N,
+            "launch": f"CUDA graph of {C} steps (copy in, GEMM, copy out per step), {reps} replays",
+            "eager_us_per_step": eager_us}
 
 
 def time_read_ceiling(dev, nbytes=1 << 30, reps=20):

@@ -35,14 +35,15 @@
 //    - activation producer (one thread): per stage two 2-D tensor-map boxes of fp16 activations
 //      (64 k x N_mma rows each, 128-byte swizzle: the MMA's B operand as it lands) into a short
 //      ring that the MMAs free;
-//    - sixteen converter warps: the weight rows go into tensor memory as the fp16 A operand
-//      (tcgen05.st, lane = row, one packed 16-byte chunk per thread and store).  The same warps
-//      retire each stage once its MMAs have completed (they wait for that anyway before reusing
-//      its tensor-memory slot): at the end of a period
-//      they read the accumulators out and keep int32 sums in registers (each warp one lane
-//      quarter and one quarter of the columns), and at the end of a segment they store bf16 or
-//      add the split tile's partial and, as the last arrival, finish it;
-//    - one or two MMA-issuing threads (two take alternate k-steps into their own accumulators).
+//    - sixteen converter warps in four groups: group g writes the weight rows of every stage
+//      q with q % 4 == g into tensor-memory A slot g as the fp16 A operand (tcgen05.st, lane =
+//      row, one packed 16-byte chunk per thread and store), so four stages convert at once.  All
+//      sixteen read the accumulators out at the end of each period (512 k), once its MMAs have
+//      completed, and keep int32 sums in registers (each warp one lane quarter and one quarter of
+//      the columns); at the end of a segment they store bf16 or add the split tile's partial and,
+//      as the last arrival, finish it;
+//    - one or two MMA-issuing threads (two take alternate k-steps into their own accumulators);
+//      a period's last MMAs signal the read-out, and the read-out frees the accumulator buffer.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -63,6 +64,11 @@ constexpr int kHalfBytes = kStageUnits * kPackSlab;  // one packed tile's share 
 constexpr int kWStage = 2 * kHalfBytes;              // 16 KiB of weight per stage
 constexpr int kConvWarps = 16;                       // four per tensor-memory lane quarter
 constexpr int kConvThreads = 32 * kConvWarps;
+// The converter warps form four groups of four (one warp per lane quarter each); group g converts
+// every stage q with q % 4 == g, whole, into tensor-memory A slot g.  Four stages are then
+// converted at once, and a warp meets the pipeline's barriers once per four stages.
+constexpr int kConvGroups = 4;
+constexpr int kGroupWarps = kConvWarps / kConvGroups;
 constexpr int kWProducerWarp = kConvWarps;           // streams the packed weight
 constexpr int kBProducerWarp = kConvWarps + 1;       // loads the activation boxes
 constexpr int kMmaWarp = kConvWarps + 2;             // first MMA-issuing warp; owns tensor memory
@@ -84,7 +90,7 @@ struct TcLayout {
   // it holds the bytes in flight from HBM.  The activation ring (from L2) is freed by the MMAs.
   static constexpr int kWStages = kN <= 64 ? 10 : 8;
   static constexpr int kBStages = kN <= 64 ? 4 : 3;
-  static constexpr int kOpStages = kN <= 64 ? 4 : 3;  // tensor-memory ring of converted weight
+  static constexpr int kOpStages = kConvGroups;       // tensor-memory A slots: one per converter group
   static constexpr int kBBox = kN * 128;              // one fp16 activation box (1 KiB multiple)
   static constexpr int kBStage = 2 * kBBox;
   static constexpr int kDCol0 = kOpStages * kACols;   // first accumulator column
@@ -181,42 +187,20 @@ __device__ __forceinline__ uint16_t epilogue(int acc, float xsv, float wsv) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-// Bounded wait for the phase of `parity` that polls with the non-blocking mbarrier.test_wait.  Every
-// role of this kernel blocks on a barrier once or more per stage, and the same kernel with its
-// waits suspended in mbarrier.try_wait was measured slower (gate_up-sized 90 us against 68 us
-// polling), so these waits poll;
-// a short sleep between polls keeps the polling warps from taking the issue slots that the
-// working warps (above all the MMA-issuing thread) need.  Gives up when another thread has
-// raised *abort, or after kWaitTimeoutCycles (then records the timeout in *status and raises
-// *abort).  Returns true when the phase completed.
-constexpr unsigned kPollSleepNs = 32;
+// Bounded wait for the phase of `parity`: mbar_wait (one non-blocking test, then suspended
+// try_wait polls that leave the issue slots to the working warps).  With converter groups (each
+// warp meets the pipeline's barriers once per four stages) suspended waits measured faster than
+// polling with short sleeps (gate_up-sized M = 64 58.0 -> 55.0 us, M = 128 70.6 -> 68.2 us); with
+// every warp converting every stage they had measured slower.  Gives up when another thread has
+// raised *abort, or after `limit` cycles (then records the timeout in *status and raises *abort).
+// Returns true when the phase completed.
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* status,
                                         long long limit = kWaitTimeoutCycles) {
-  const long long t0 = clock64();
-  for (int n = 0;; ++n) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    if (done) return true;
-    __nanosleep(kPollSleepNs);
-    if ((n & 63) == 63) {
-      if (*abort) return false;
-      if (clock64() - t0 > limit) {
-        atomicOr(status, W8A8_DEV_WAIT_TIMEOUT);
-        *abort = 1;
-        return false;
-      }
-    }
-  }
+  return mbar_wait(bar, parity, abort, status, limit);
 }
 
 // tc_wait taken by a whole warp: the warp goes on only if every lane saw the phase complete, so
-// the warp-wide tensor-memory instructions after it always run with all 32 lanes.  (Suspended
-// waits in the converter warps, which would leave their issue slots to the MMA-issuing thread,
-// were measured slower: gate_up-sized 68 -> 90 us.)
+// the warp-wide tensor-memory instructions after it always run with all 32 lanes.
 __device__ __forceinline__ bool mbar_wait_all(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* status) {
   const bool ok = tc_wait(bar, parity, abort, status);
   return __all_sync(0xffffffffu, ok) != 0;
@@ -296,7 +280,8 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
   __shared__ __align__(8) uint64_t bfull_bar[NB];   // an activation stage (two boxes) landed
   __shared__ __align__(8) uint64_t bdone_bar[NB];   // the MMAs reading an activation stage completed
   __shared__ __align__(8) uint64_t adone_bar[NA];   // the MMAs reading a tensor-memory A stage completed
-  __shared__ __align__(8) uint64_t conv_bar[NA];    // a tensor-memory A stage written (its activations landed)
+  __shared__ __align__(8) uint64_t conv_bar[NA];    // a tensor-memory A stage written by its converter group
+  __shared__ __align__(8) uint64_t dfull_bar[2];    // the MMAs of an accumulation period completed
   __shared__ __align__(8) uint64_t dempty_bar[2];   // an accumulator buffer has been read out
   __shared__ __align__(8) uint64_t final_bar[kI];   // every MMA of an issuer completed
   __shared__ __align__(8) uint64_t sync_bar;        // converter warps meet at a split tile's combine
@@ -316,7 +301,7 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
 #pragma unroll
     for (int s = 0; s < NW; ++s) {
       mbar_init(&wfull_bar[s], 1);
-      mbar_init(&wempty_bar[s], kConvWarps);
+      mbar_init(&wempty_bar[s], kGroupWarps);
     }
 #pragma unroll
     for (int s = 0; s < NB; ++s) {
@@ -326,10 +311,13 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
 #pragma unroll
     for (int a = 0; a < NA; ++a) {
       mbar_init(&adone_bar[a], kI);
-      mbar_init(&conv_bar[a], kConvWarps);
+      mbar_init(&conv_bar[a], kGroupWarps);
     }
 #pragma unroll
-    for (int d = 0; d < 2; ++d) mbar_init(&dempty_bar[d], kConvWarps);
+    for (int d = 0; d < 2; ++d) {
+      mbar_init(&dfull_bar[d], kI);
+      mbar_init(&dempty_bar[d], kConvWarps);
+    }
 #pragma unroll
     for (int i = 0; i < kI; ++i) mbar_init(&final_bar[i], 1);
     mbar_init(&sync_bar, kConvWarps);
@@ -405,9 +393,9 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
         if (it.period_first() && it.period >= 2 &&
             !tc_wait(&dempty_bar[db], (uint32_t)(((it.period >> 1) - 1) & 1), &abort_flag, p.status))
           break;
-        // The converter warps saw the activation stage land before they finished the A stage: one
-        // wait covers both operands.
+        // Both operands: the A slot written by its converter group, the activation stage landed.
         if (!tc_wait(&conv_bar[a], (uint32_t)((it.q / NA) & 1), &abort_flag, p.status)) break;
+        if (!tc_wait(&bfull_bar[sb], (uint32_t)((it.q / NB) & 1), &abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_addr = tmem + (uint32_t)(L::kDCol0 + (issuer * 2 + db) * kN);
         const uint32_t a_addr = tmem + (uint32_t)(a * kACols);
@@ -426,6 +414,7 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
         // may read the accumulators.
         umma_commit(&bdone_bar[sb]);
         umma_commit(&adone_bar[a]);
+        if (it.period_last()) umma_commit(&dfull_bar[db]);
       }
       // Whatever happened above, every MMA this thread issued completes before tensor memory is freed.
       umma_commit(&final_bar[issuer]);
@@ -433,13 +422,16 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
     }
   } else {
     // ---------------------------------------------------------------- converter warps
-    // Warp w owns tensor-memory lanes 32 (w % 4) ... + 31 (rows of the CTA tile), unit w / 4 of every
-    // stage, and accumulator columns (w / 4) kN / 4 ... + kN / 4 - 1.  Its 32 rows are two 16-row
-    // groups s of packed tile (w % 4) / 2; the packed 16-byte chunk (s, lane) holds k = 8c ... 8c + 7
-    // of rows g and g + 8 (g = lane / 4, c = lane % 4; words: row g k 8c.., row g + 8 k 8c.., row g
-    // k 8c+4.., row g + 8 k 8c+4..), which is what the 16x256b store takes from thread `lane`: one
-    // 16-byte read (a group is 512 contiguous bytes), four exact conversions, one store per group.
-    const int quad = warp & 3, unit = warp >> 2;
+    // Warp w owns tensor-memory lanes 32 (w % 4) ... + 31 (rows of the CTA tile) and accumulator
+    // columns (w / 4) kN / 4 ... + kN / 4 - 1, and converts its 32 rows of every stage q with
+    // q % 4 == w / 4 (its group), all units of the stage, into A slot w / 4.  Its 32 rows are two
+    // 16-row groups s of packed tile (w % 4) / 2; the packed 16-byte chunk (s, lane) of a unit holds
+    // k = 8c ... 8c + 7 of rows g and g + 8 (g = lane / 4, c = lane % 4; words: row g k 8c.., row
+    // g + 8 k 8c.., row g k 8c+4.., row g + 8 k 8c+4..), which is what the 16x256b store takes from
+    // thread `lane`: one 16-byte read (a group is 512 contiguous bytes), four exact conversions, one
+    // store per group and unit.  Every warp reads out every accumulation period (its columns of its
+    // lanes), four stages after the period's last one.
+    const int quad = warp & 3, unit = warp >> 2;   // unit: the converter group, and the column quarter
     const int half = quad >> 1;
     const int s16 = 2 * (quad & 1);
     const uint32_t t_lane = tmem + ((uint32_t)(32 * quad) << 16);
@@ -464,6 +456,7 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
       if (dr.seg_first()) wsv = n < p.N ? __ldg(p.w_scale + n) : 0.f;
       if (dr.period_last()) {
         const int db = dr.period & 1;
+        if (!mbar_wait_lane0(&dfull_bar[db], (uint32_t)((dr.period >> 1) & 1), &abort_flag, p.status)) return false;
         tc_fence_after();
 #pragma unroll
         for (int i = 0; i < kI; ++i) {
@@ -547,55 +540,51 @@ __global__ void __launch_bounds__(TcLayout<NT16>::kThreads, 1) w8a8_gemm_tc_kern
       ok = false;
     }
     for (Walk it(b0, b1, p.KB); ok && !it.done(); it.next()) {
+      // Stage q - 4 retires as the walk passes stage q: at a period's end this reads the period's
+      // accumulators once its MMAs have completed.
+      if (it.q >= kConvGroups && !retire()) {
+        ok = false;
+        break;
+      }
+      if ((it.q & (kConvGroups - 1)) != unit) continue;   // another group converts this stage
       const int s = it.q % NW;
-      const int a = it.q % NA;
+      const int a = unit;   // this group's A slot
       if (!mbar_wait_all(&wfull_bar[s], (uint32_t)((it.q / NW) & 1), &abort_flag, p.status)) {
         ok = false;
         break;
       }
-      if (it.q >= NA) {
-        // The A stage is free once the MMAs of stage q - NA have completed; that stage retires now.
-        const int qo = it.q - NA;
-        if (!mbar_wait_lane0(&adone_bar[a], (uint32_t)((qo / NA) & 1), &abort_flag, p.status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (!retire()) {
-          ok = false;
-          break;
-        }
+      // The A slot is free once the MMAs of the group's previous stage, q - 4, have completed.
+      if (it.q >= kConvGroups &&
+          !mbar_wait_lane0(&adone_bar[a], (uint32_t)(((it.q - kConvGroups) / NA) & 1), &abort_flag, p.status)) {
+        ok = false;
+        break;
       }
+      tc_fence_after();
       const bool have = 2 * it.t + half < p.tiles64;   // this packed tile exists (warp-uniform)
-      if (have && unit < it.ns) {
-        const uint8_t* wsrc = wring + s * kWStage + half * kHalfBytes + unit * kPackSlab;
+      if (have) {
+        const uint8_t* wsrc = wring + s * kWStage + half * kHalfBytes;
+        for (int u = 0; u < it.ns; ++u) {
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const uint4 u = lds128(wsrc + ((s16 + r) * 32 + lane) * 16);
-          uint32_t h[8];
-          offset_bytes_to_half2_pairs(u.x, h[0], h[1]);   // row g,     k 8c .. 8c+3
-          offset_bytes_to_half2_pairs(u.y, h[2], h[3]);   // row g + 8, k 8c .. 8c+3
-          offset_bytes_to_half2_pairs(u.z, h[4], h[5]);   // row g,     k 8c+4 .. 8c+7
-          offset_bytes_to_half2_pairs(u.w, h[6], h[7]);   // row g + 8, k 8c+4 .. 8c+7
-          tmem_st_16x256_x2(t_lane + ((uint32_t)(16 * r) << 16) + (uint32_t)(a * kACols + 16 * unit), h);
+          for (int r = 0; r < 2; ++r) {
+            const uint4 w = lds128(wsrc + u * kPackSlab + ((s16 + r) * 32 + lane) * 16);
+            uint32_t h[8];
+            offset_bytes_to_half2_pairs(w.x, h[0], h[1]);   // row g,     k 8c .. 8c+3
+            offset_bytes_to_half2_pairs(w.y, h[2], h[3]);   // row g + 8, k 8c .. 8c+3
+            offset_bytes_to_half2_pairs(w.z, h[4], h[5]);   // row g,     k 8c+4 .. 8c+7
+            offset_bytes_to_half2_pairs(w.w, h[6], h[7]);   // row g + 8, k 8c+4 .. 8c+7
+            tmem_st_16x256_x2(t_lane + ((uint32_t)(16 * r) << 16) + (uint32_t)(a * kACols + 16 * u), h);
+          }
         }
       }
       // Every weight value of the stage has been read and used: the slot goes back to the producer.
       __syncwarp();
       if (lane == 0) mbar_arrive(&wempty_bar[s]);
-      // The MMAs of this stage also need its activations: see them land before handing the stage over.
-      if (!mbar_wait_all(&bfull_bar[it.q % NB], (uint32_t)((it.q / NB) & 1), &abort_flag, p.status)) {
-        ok = false;
-        break;
-      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive_warp(&conv_bar[a]);
     }
     // Retire the stages still in flight.
     while (ok && !dr.done()) {
-      if (!mbar_wait_lane0(&adone_bar[dr.q % NA], (uint32_t)((dr.q / NA) & 1), &abort_flag, p.status)) break;
-      tc_fence_after();
       if (!retire()) break;
     }
   }

@@ -14,10 +14,12 @@ CTA runs the library's own split plans produce, and checks that
   * every role finishes (no deadlock), and
   * every stage is converted, multiplied and retired once, every period's accumulator read once.
 
-Roles (one CTA): the weight producer, the activation producer, sixteen converter warps as in the
-kernel (each arrives once per warp), I issuing threads, and an MMA engine that completes each
-issuer's commits in order.  Ring depths are the kernel's (weight 8 / activations 3 / tensor-memory A 3 at N = 128,
-10 / 4 / 4 with two issuers at N = 64).
+Roles (one CTA): the weight producer, the activation producer, sixteen converter warps in four
+groups as in the kernel (group g converts the stages q with q % 4 == g into A slot g; every warp
+reads out every accumulation period; each arrives once per warp), I issuing threads, and an MMA
+engine that completes each issuer's commits in order.  Ring depths are the kernel's (weight 8 /
+activations 3 at N = 128, 10 / 4 with two issuers at N = 64; four A slots, two accumulator
+buffers).
 """
 import random
 
@@ -82,14 +84,17 @@ class Walk:
 
 def _run_cta(b0, b1, KB, n_mma, seed, fault=None):
     rng = random.Random(seed)
-    NW, NB, NA, kI = (10, 4, 4, 2) if n_mma == 64 else (8, 3, 3, 1)
+    NW, NB, kI = (10, 4, 2) if n_mma == 64 else (8, 3, 1)
+    NA = GROUPS = 4   # A slots, one per converter group
     C = 16  # converter warps, as many as the kernel runs (one arrival per warp)
+    GW = C // GROUPS
     wfull = [Barrier(f"wfull{s}", 1) for s in range(NW)]
-    wempty = [Barrier(f"wempty{s}", C) for s in range(NW)]
+    wempty = [Barrier(f"wempty{s}", GW) for s in range(NW)]
     bfull = [Barrier(f"bfull{s}", 1) for s in range(NB)]
     bdone = [Barrier(f"bdone{s}", kI) for s in range(NB)]
     adone = [Barrier(f"adone{a}", kI) for a in range(NA)]
-    conv = [Barrier(f"conv{a}", C) for a in range(NA)]
+    conv = [Barrier(f"conv{a}", GW) for a in range(NA)]
+    dfull = [Barrier(f"dfull{d}", kI) for d in range(2)]
     dempty = [Barrier(f"dempty{d}", C) for d in range(2)]
     sync = Barrier("sync", C)
     pending_commits = [[] for _ in range(kI)]   # per issuer, in issue order: barriers to arrive on
@@ -102,7 +107,7 @@ def _run_cta(b0, b1, KB, n_mma, seed, fault=None):
             s = q % NW
             if q >= NW and fault != "weight producer skips its wait":
                 yield from wait(wempty[s], ((q // NW) & 1) ^ 1, q // NW - 1)
-            # overwriting slot s: every converter warp has read stage q - NW
+            # overwriting slot s: the group that converts stage q - NW has read it
             assert q < NW or wempty[s].completed >= q // NW, "weight slot overwritten before it was read"
             wfull[s].arrive()   # expect_tx + copies; the bytes land eventually
             it.next()
@@ -129,8 +134,11 @@ def _run_cta(b0, b1, KB, n_mma, seed, fault=None):
                 yield from wait(dempty[db], ((it.period >> 1) - 1) & 1, (it.period >> 1) - 1)
             parity = (it.q // NA) & 1
             yield from wait(conv[a], parity ^ 1 if fault == "issuer waits on the wrong parity" else parity, it.q // NA)
+            if fault != "issuer skips the activation wait":
+                yield from wait(bfull[sb], (it.q // NB) & 1, it.q // NB)
             # the MMAs read A slot a and activation slot sb of this stage, and write buffer db
-            assert conv[a].completed >= it.q // NA + 1 and bfull[sb].completed >= it.q // NB + 1
+            assert conv[a].completed >= it.q // NA + 1, "A slot read before its group wrote it"
+            assert bfull[sb].completed >= it.q // NB + 1, "activation slot read before it landed"
             assert it.period < 2 or not it.period_first() or dempty[db].completed >= it.period >> 1, \
                 "accumulator buffer overwritten before its read-out"
             steps = [j for j in range(i, 2 * it.ns, kI)]
@@ -138,6 +146,8 @@ def _run_cta(b0, b1, KB, n_mma, seed, fault=None):
             log["issued"][i].append(it.q)
             pending_commits[i].append(bdone[sb])
             pending_commits[i].append(adone[a])
+            if it.period_last():
+                pending_commits[i].append(dfull[db])
             it.next()
             yield
 
@@ -151,14 +161,17 @@ def _run_cta(b0, b1, KB, n_mma, seed, fault=None):
 
     def converter(w):
         sync_phase = 0
+        group = w // GW
         dr = Walk(b0, b1, KB)
 
         def retire():
             nonlocal sync_phase
-            # reading the accumulators (or just passing the stage) after its MMAs have completed
-            assert adone[dr.q % NA].completed >= dr.q // NA + 1, "stage retired before its MMAs completed"
             log["retired"][w].append(dr.q)
             if dr.period_last():
+                # reading the period's accumulators once its MMAs have completed
+                if fault != "converter skips the read-out wait":
+                    yield from wait(dfull[dr.period & 1], (dr.period >> 1) & 1, dr.period >> 1)
+                assert dfull[dr.period & 1].completed >= (dr.period >> 1) + 1, "accumulators read before their MMAs completed"
                 log["drained"][w].append(dr.period)
                 dempty[dr.period & 1].arrive()
                 if dr.seg_last() and not dr.whole_tile():
@@ -172,25 +185,24 @@ def _run_cta(b0, b1, KB, n_mma, seed, fault=None):
 
         it = Walk(b0, b1, KB)
         while not it.done():
-            s, a = it.q % NW, it.q % NA
-            yield from wait(wfull[s], (it.q // NW) & 1, it.q // NW)
-            if it.q >= NA:
-                qo = it.q - NA
-                if fault != "converter skips the MMA wait":
-                    yield from wait(adone[a], (qo // NA) & 1, qo // NA)
+            # stage q - 4 retires as the walk passes stage q
+            if it.q >= GROUPS:
                 yield from retire()
-            # writing A slot a: the MMAs of stage q - NA, which read it, have completed
-            assert it.q < NA or adone[a].completed >= (it.q - NA) // NA + 1, "A slot overwritten under the MMAs"
-            assert wfull[s].completed >= it.q // NW + 1
-            if w == 0:
-                log["converted"].append(it.q)
-            wempty[s].arrive()
-            yield from wait(bfull[it.q % NB], (it.q // NB) & 1, it.q // NB)
-            conv[a].arrive()
+            if it.q % GROUPS == group:
+                s, a = it.q % NW, group
+                yield from wait(wfull[s], (it.q // NW) & 1, it.q // NW)
+                if it.q >= GROUPS and fault != "converter skips the MMA wait":
+                    yield from wait(adone[a], ((it.q - GROUPS) // NA) & 1, (it.q - GROUPS) // NA)
+                # writing A slot a: the MMAs of stage q - 4, which read it, have completed
+                assert it.q < NA or adone[a].completed >= (it.q - NA) // NA + 1, "A slot overwritten under the MMAs"
+                assert wfull[s].completed >= it.q // NW + 1
+                if w == group * GW:
+                    log["converted"].append(it.q)
+                wempty[s].arrive()
+                conv[a].arrive()
             it.next()
             yield
         while not dr.done():
-            yield from wait(adone[dr.q % NA], (dr.q // NA) & 1, dr.q // NA)
             yield from retire()
 
     done_issuers = [False] * kI
@@ -209,7 +221,7 @@ def _run_cta(b0, b1, KB, n_mma, seed, fault=None):
             periods += 1
         walk.next()
         stages += 1
-    assert log["converted"] == list(range(stages))
+    assert sorted(log["converted"]) == list(range(stages))
     for i in range(kI):
         assert log["issued"][i] == list(range(stages))
     for w in range(C):
@@ -234,7 +246,8 @@ def test_protocol_has_no_aliasing_and_no_deadlock(M, K, N, blocks):
 
 
 FAULTS = ["weight producer skips its wait", "activation producer skips its wait", "issuer skips the read-out wait",
-          "issuer waits on the wrong parity", "converter skips the MMA wait"]
+          "issuer waits on the wrong parity", "issuer skips the activation wait", "converter skips the MMA wait",
+          "converter skips the read-out wait"]
 
 
 @pytest.mark.parametrize("fault", FAULTS)
