@@ -331,7 +331,7 @@ def time_gemm(M, K, N, dist, seed, steps, warmup, blocks=0, device=None, sample_
     step_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
     total_ms = max_over_ranks(evs[0].elapsed_time(evs[-1]))
     per_call_us = sorted(s * 1e3 / C for s in step_ms)
-    plan = lib8.w8a8_plan(M, K, N, blocks)
+    plan = lib8.w8a8_plan(M, K, N, blocks, flags=flags)
     res = {
         "R": R, "C": C, "wbytes": wbytes, "total_ms": total_ms, "steps": steps,
         "kernel": (f"w8a8_gemm_tc_kernel<{plan['n8_tiles'] // 2}>" if plan["tensor_memory"] else

@@ -66,13 +66,18 @@ enum {
 
 /* Launch flags of w8a8_gemm and q8_0_gemv. */
 enum {
-    /* Programmatic dependent launch: the kernel may become resident, and start streaming the packed
-     * weight (W_packed, or q and d of q8_0_gemv), while the work queued before it on the stream is
-     * still running; every other input, the output and the workspace are touched only after that
-     * work has completed and its memory is visible.  The caller guarantees that the weight buffers
-     * are not written by work still in flight on the stream (weights are load-time constants: pack
-     * them, then synchronise once).  Consecutive calls then overlap one call's weight prefetch with
-     * the previous call's tail, inside a CUDA graph as well. */
+    /* Every w8a8_gemm decode launch (M <= 32, and the row chunks of larger M) and every q8_0_gemv
+     * launch is a programmatic dependent of the work queued before it on the stream, flag or not:
+     * its CTAs may become resident and set themselves up while the previous kernel finishes, and
+     * touch no global memory until that kernel has completed and its writes are visible.  This
+     * needs nothing from the caller and behaves as plain stream order.
+     * W8A8_FLAG_PDL (programmatic dependent launch with weight prefetch) also lets the kernel start
+     * streaming the packed weight (W_packed, or q, d and gamma of q8_0_gemv) before that point;
+     * every other input, the output and the workspace are still touched only after it.  The caller
+     * guarantees that the weight buffers are not written by work still in flight on the stream
+     * (weights are load-time constants: pack them, then synchronise once).  Consecutive calls then
+     * overlap one call's weight prefetch with the previous call's tail, inside a CUDA graph as
+     * well. */
     W8A8_FLAG_PDL = 1u,
     /* w8a8_gemm with 32 < M <= 128: always run the tcgen05 arm.  Without it the automatic plan
      * (blocks == 0) runs, whichever a cost model measured on GB300 predicts faster, either that

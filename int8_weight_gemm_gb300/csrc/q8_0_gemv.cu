@@ -48,6 +48,7 @@ struct Q8Params {
   float4* partials;
   int T, K, N, KB, warps, splits;
   int cluster;      // > 1: CTA r of a tile's cluster runs the tile's warps r * warps .. r * warps + warps - 1
+  int pdl;          // W8A8_FLAG_PDL: the weights may be read before the dependency wait
   int tile_warps;   // warps of a tile in all (the k-block runs)
 };
 
@@ -101,9 +102,13 @@ __global__ void __launch_bounds__(32 * kQ8MaxWarps) q8_0_gemv_kernel(const __gri
   const int n_a = tile * 16 + g, n_b = n_a + 8;
 
   pdl_trigger();
+  // Every launch is a programmatic dependent of the work before it (q8_launch): without
+  // W8A8_FLAG_PDL nothing global is read before the dependency wait, after which the previous
+  // kernel's writes are visible.
+  if (!p.pdl) pdl_wait();
   // Issue every load of this warp's run first: the read is latency-bound, not bandwidth-bound.
-  // The quants and scales are weights (never written by the work this call depends on), so they
-  // are requested before the dependency wait; the activations after it.
+  // With W8A8_FLAG_PDL the quants and scales, weights that nothing in flight writes (the caller's
+  // promise), are requested before the dependency wait; the activations after it.
   uint2 qa[kQ8MaxBlocksPerWarp], qb[kQ8MaxBlocksPerWarp];
   uint4 xv[kQ8MaxBlocksPerWarp], gv[kQ8MaxBlocksPerWarp];
   uint16_t da[kQ8MaxBlocksPerWarp], db[kQ8MaxBlocksPerWarp];
@@ -348,18 +353,19 @@ cudaError_t q8_launch(const Q8Plan& pl, const void* x, const int8_t* q, const vo
   p.splits = pl.splits;
   p.cluster = pl.cluster;
   p.tile_warps = pl.tile_warps;
+  p.pdl = pdl ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)pl.blocks);
   cfg.blockDim = dim3((unsigned)(32 * pl.warps));
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
+  // Always a programmatic dependent of the work before it (see the kernel: without the flag nothing
+  // global is touched before the dependency wait).
   cudaLaunchAttribute attr[2];
   unsigned n = 0;
-  if (pdl) {
-    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[n].val.programmaticStreamSerializationAllowed = 1;
-    ++n;
-  }
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
   if (pl.cluster > 1) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
     attr[n].val.clusterDim.x = (unsigned)pl.cluster;

@@ -173,3 +173,34 @@ def test_pdl_launch_matches_plain_launch_bitwise(K, N):
     for o in outs:
         np.testing.assert_array_equal(bf16_bits(o), plain)
     _check(c)
+
+
+@pytest.mark.parametrize("K,N", [(4096, 320), (8192, 64)])
+def test_weights_rewritten_just_before_a_read_are_the_ones_read(K, N):
+    # Every read is launched as a programmatic dependent of the work before it; without
+    # W8A8_FLAG_PDL it must still behave as plain stream order.  The quants, scales and activations
+    # are overwritten on the stream right before each read, with no synchronisation: a read that
+    # fetched its weights before those copies had finished would see the old values.  Each output
+    # is checked against the oracle of the inputs it should have read (both bounds).
+    a, b = Q8Case(4, K, N, seed=91), Q8Case(4, K, N, seed=92)
+    dst = Q8Case(4, K, N, seed=93)
+    bounds = []
+    for src in (a, b):
+        ref, stated = src.reference()
+        xb, db = src.bits()
+        bounds.append((ref, stated, tight_bound(xb, src.q, db)))
+    torch.cuda.synchronize()
+    outs = []
+    for i in range(6):
+        src = (a, b)[i % 2]
+        dst.qd.copy_(src.qd)
+        dst.dd.copy_(src.dd)
+        dst.xd.copy_(src.xd)
+        outs.append(dst.run())
+    torch.cuda.synchronize()
+    for i, o in enumerate(outs):
+        ref, stated, tight = bounds[i % 2]
+        err = np.abs(o.float().cpu().numpy().astype(np.float64) - ref)
+        assert (err <= stated).all() and (err <= tight).all(), f"read {i}: max err/tight bound {(err / tight).max():.3g}"
+        np.testing.assert_array_equal(bf16_bits(o), bf16_bits(outs[i % 2]))
+    assert lib8.w8a8_workspace_status(dst.ws) == 0

@@ -195,6 +195,40 @@ def test_a_changed_weight_byte_changes_exactly_its_column():
     assert set(changed.tolist()) <= {77}
 
 
+@pytest.mark.parametrize("M,K,N,blocks", [(16, 4096, 1536, 0), (5, 2048, 4096, 7), (32, 1024, 520, 0)])
+def test_weights_rewritten_just_before_a_call_are_the_ones_read(M, K, N, blocks):
+    # Every call is launched as a programmatic dependent of the work before it; without
+    # W8A8_FLAG_PDL it must still behave as plain stream order.  Here the packed weight buffer is
+    # repacked with new values by the kernel right before each call, on the same stream, with no
+    # synchronisation: a call that read its weight before the pack had finished would see the old
+    # values.  The activations and scales are rewritten the same way.
+    x, xs, W, ws = synth.w8a8_inputs(M, K, N, seed=M + K + N)
+    x2, xs2, W2, ws2 = synth.w8a8_inputs(M, K, N, seed=M + K + N + 1)
+    dev = torch.device("cuda")
+    xd = torch.from_numpy(x).to(dev)
+    xsd = torch.from_numpy(xs).to(dev)
+    wsd = torch.from_numpy(ws).to(dev)
+    Wd = [torch.from_numpy(W).to(dev), torch.from_numpy(W2).to(dev)]
+    srcs = [(torch.from_numpy(x).to(dev), torch.from_numpy(xs).to(dev), torch.from_numpy(ws).to(dev)),
+            (torch.from_numpy(x2).to(dev), torch.from_numpy(xs2).to(dev), torch.from_numpy(ws2).to(dev))]
+    refs = [oracle.w8a8_gemm(x, xs, W, ws), oracle.w8a8_gemm(x2, xs2, W2, ws2)]
+    wsp = lib8.alloc_workspace(lib8.w8a8_workspace_bytes(M, K, N, blocks), dev)
+    Wp = lib8.w8a8_pack_weights(Wd[0], ws=wsp)
+    torch.cuda.synchronize()
+    outs = []
+    for i in range(6):
+        j = i % 2
+        lib8.w8a8_pack_weights(Wd[j], W_packed=Wp)       # rewrites the whole packed weight
+        xd.copy_(srcs[j][0])
+        xsd.copy_(srcs[j][1])
+        wsd.copy_(srcs[j][2])
+        outs.append(lib8.w8a8_gemm(xd, xsd, Wp, wsd, wsp, N, blocks=blocks))
+    torch.cuda.synchronize()
+    for i, o in enumerate(outs):
+        np.testing.assert_array_equal(bf16_bits(o), refs[i % 2])
+    assert lib8.w8a8_workspace_status(wsp) == 0
+
+
 @pytest.mark.parametrize("blocks", [0, 7, 3072])
 def test_pdl_calls_back_to_back_are_bit_identical(blocks):
     # Programmatic dependent launch: consecutive calls overlap (the next call prefetches its weight
