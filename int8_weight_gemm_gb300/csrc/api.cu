@@ -93,14 +93,15 @@ cudaError_t encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType type, voi
 // and by the tensor-memory kernel's MMA width.  The decode kernel's per-byte cost grows with M (its
 // MMA and activation-conversion work per weight byte do), the tensor-memory kernel's much less, so
 // row chunks win on small weights and the tensor-memory kernel on large ones.  The decode lines fit
-// within 7 %; the tensor-memory kernel's times depend on how its tiles fall over the SMs and fit
-// only within 22 %, so the choice can miss near the crossover (by at most 7 us on the measured
-// shapes, against 20 us for the lines this model replaced).
+// within 8 %; the tensor-memory kernel's times depend on how its tiles fall over the SMs and fit
+// only within 22 %, yet on the 24 measured (shape, M) points the lines pick the faster arm every
+// time (fitted again after the decode launches became programmatic dependents and the
+// tensor-memory converters moved to stage groups).
 static double decode_cost_us(int nt8, double w_mib) {
-  static const double fixed[5] = {0.0, 3.97, 4.77, 4.31, 4.67}, per_mib[5] = {0.0, 0.150, 0.164, 0.298, 0.333};
+  static const double fixed[5] = {0.0, 3.18, 3.97, 3.87, 4.19}, per_mib[5] = {0.0, 0.150, 0.164, 0.267, 0.306};
   return fixed[nt8] + per_mib[nt8] * w_mib;
 }
-static double tc_cost_us(int M, double w_mib) { return M <= 64 ? 17.79 + 0.451 * w_mib : 29.87 + 0.459 * w_mib; }
+static double tc_cost_us(int M, double w_mib) { return M <= 64 ? 17.28 + 0.422 * w_mib : 27.75 + 0.463 * w_mib; }
 
 int any_plan(int M, int K, int N, int blocks, int sm_count, AnyPlan* plan, bool force_tc) {
   plan->tc = false;
