@@ -823,6 +823,10 @@ def run_sweep(args):
     shapes += [(M, K, N, "uniform", 5000 + M) for (N, K) in ((1536, 4096), (2560, 4096), (4096, 2048))
                for M in (64, 128)]
     shapes += [(128, 4096, 24576, "mlp", 5), (128, 12288, 4096, "mlp", 5), (48, 4096, 1536, "uniform", 5048)]
+    # more tile-aligned decode shapes (CTA-count rule of the automatic plan)
+    shapes += [(16, 4096, 8192, "mlp", 4), (16, 4096, 12288, "mlp", 4), (16, 4096, 6144, "mlp", 4),
+               (16, 14336, 4096, "mlp", 4), (1, 12288, 4096, "mlp", 4), (32, 12288, 4096, "mlp", 4),
+               (32, 4096, 1536, "uniform", 1)]
     if args.shapes:
         shapes = [shapes[int(i)] for i in args.shapes.split(",")]
     peak, _ = _peaks()

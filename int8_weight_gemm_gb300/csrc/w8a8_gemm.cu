@@ -736,10 +736,19 @@ int gemm_plan(int M, int K, int N, int blocks, int sm_count, GemmPlan* plan) {
   pl.kb = K / kKBlock;
   pl.slabs = (long long)pl.n_tiles * pl.kb;
   if (blocks == 0) {
-    // Two CTAs on every SM: measured fastest for every workload shape once the split-tile
-    // combine costs one round trip (fewer CTAs stream slower and save little in the combine).
+    // Up to two CTAs on every SM (the most that fit): fewer CTAs than tiles stream slower and save
+    // little in the split-tile combine, which costs one round trip.
     const long long g = (long long)kAutoCtasPerSm * (sm_count > 0 ? sm_count : 152);
-    pl.blocks = (int)(g < pl.slabs ? g : pl.slabs);
+    long long gg = g < pl.slabs ? g : pl.slabs;
+    // At M <= 16, with a CTA or more per tile, every tile is cut into the same number of parts
+    // (the largest multiple of the tile count that fits): the longest part is no longer, so no
+    // CTA streams more than with the extra CTAs, and the HBM share of each CTA grows.  Measured
+    // on GB300 (M = 16, graph replays): K = 12288, N = 4096 12.24 -> 11.54 us (256 CTAs), K = 4096,
+    // N = 8192 9.51 -> 9.08 (256), N = 12288 12.60 -> 12.20 (192), N = 1536 4.69 -> 4.65 (288);
+    // 11 of 12 shapes faster.  At M = 32 the consumer warps, not the stream, set the pace, and the
+    // extra CTAs win (K = 12288, N = 4096: 18.52 against 19.10 us), so larger M keeps them.
+    if (pl.nt8 <= 2 && gg >= pl.n_tiles) gg = (long long)pl.n_tiles * (gg / pl.n_tiles);
+    pl.blocks = (int)gg;
   } else {
     if (blocks > pl.slabs) return W8A8_ERR_INVALID_ARG;
     pl.blocks = blocks;
