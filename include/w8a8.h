@@ -169,8 +169,10 @@ int w8a8_pack_weights(const int8_t* W, int K, int N, void* W_packed, void* ws, s
  *           equal length to within one slab, one per CTA, so no CTA spans two tiles; with
  *           blocks < T the tiles are laid end to end and CTA i takes a contiguous run of
  *           ceil or floor(T KB / (u blocks)) units of u slabs (the longer runs first), u being
- *           the plan's split_unit (1 or 4; see w8a8_plan_t).  0 = automatic (twice
- *           the SM count, at most one CTA per slab).  Must not exceed the number of slabs.
+ *           the plan's split_unit (1 or 4; see w8a8_plan_t).  0 = automatic: twice the SM
+ *           count, at most one CTA per slab; for M <= 16 with that count >= T, rounded down to a
+ *           multiple of T so that every tile is cut into the same number of parts.  Must not
+ *           exceed the number of slabs.
  *           For M > 32 the same rule applies to T = ceil(N/128) tiles of 128 rows (two packed
  *           tiles each) x KB units of 32 k, with one CTA per SM by default.
  *  flags    0, W8A8_FLAG_PDL and/or W8A8_FLAG_TENSOR_MEMORY_ARM (W8A8_FLAG_TEST_STALL for tests
