@@ -305,6 +305,18 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// L2 prefetches.  A prefetch is a hint: it changes no value that any later read returns (device
+// memory is coherent in L2, and nothing lands in the SM), so it may be issued before a dependency
+// wait on data that the previous kernel may still write.
+// [src, src + bytes) into L2; src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+// The L2 line holding addr.
+__device__ __forceinline__ void prefetch_l2_line(const void* addr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(addr) : "memory");
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 // Wait until the grids this one depends on have completed and their memory is visible.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

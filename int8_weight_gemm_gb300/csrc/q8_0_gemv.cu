@@ -104,8 +104,22 @@ __global__ void __launch_bounds__(32 * kQ8MaxWarps) q8_0_gemv_kernel(const __gri
   pdl_trigger();
   // Every launch is a programmatic dependent of the work before it (q8_launch): without
   // W8A8_FLAG_PDL nothing global is read before the dependency wait, after which the previous
-  // kernel's writes are visible.
-  if (!p.pdl) pdl_wait();
+  // kernel's writes are visible.  Only this warp's quants and scales are prefetched into L2 first
+  // (a prefetch changes no value that a later read returns), so that the loads after the wait
+  // hit in L2: lane r < 16 the quants of row tile * 16 + r, lane 16 + r that row's scales.
+  if (!p.pdl) {
+    const int r = lane & 15;
+    const long long n = (long long)tile * 16 + r;
+    if (nb > 0 && n < p.N) {
+      if (lane < 16) {
+        bulk_prefetch_l2(p.q + n * p.K + (long long)wb0 * 32, (uint32_t)nb * 32u);
+      } else {
+        prefetch_l2_line(p.d + n * p.KB + wb0);
+        prefetch_l2_line(p.d + n * p.KB + wb1 - 1);
+      }
+    }
+    pdl_wait();
+  }
   // Issue every load of this warp's run first: the read is latency-bound, not bandwidth-bound.
   // With W8A8_FLAG_PDL the quants and scales, weights that nothing in flight writes (the caller's
   // promise), are requested before the dependency wait; the activations after it.

@@ -323,6 +323,13 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
       bulk_g2s_hint(wring + pq * L::kWStage, p.wp + (size_t)it.u * kSlabBytes, (uint32_t)(it.ns * kSlabBytes),
                     &full_bar[pq], policy);
     }
+    // Without that promise the first stages' weight bytes are only prefetched into L2, which
+    // changes nothing a later read returns; the copies after the dependency wait then hit in L2.
+    if (!p.pdl) {
+      StageIter pf(b0, b1, p.KB, kStageSlabs, kMulti);
+      for (int j = 0; j < NS && !pf.done(); pf.next(), ++j)
+        bulk_prefetch_l2(p.wp + (size_t)pf.u * kSlabBytes, (uint32_t)(pf.ns * kSlabBytes));
+    }
   }
   for (int i = threadIdx.x; i < L::kSegSumInts; i += (kMulti ? kThreads : kThreadsNoCombine)) segsum[i] = 0;
   if (threadIdx.x < 64) (&xsum_sm[0][0])[threadIdx.x] = 0;
