@@ -827,6 +827,8 @@ def run_sweep(args):
     shapes += [(16, 4096, 8192, "mlp", 4), (16, 4096, 12288, "mlp", 4), (16, 4096, 6144, "mlp", 4),
                (16, 14336, 4096, "mlp", 4), (1, 12288, 4096, "mlp", 4), (32, 12288, 4096, "mlp", 4),
                (32, 4096, 1536, "uniform", 1)]
+    shapes += [(1, 4096, 24576, "mlp", 4), (32, 4096, 24576, "mlp", 4)]
+    shapes += [(24, 4096, 2560, "uniform", 3024), (24, 2048, 4096, "uniform", 3024)]
     if args.shapes:
         shapes = [shapes[int(i)] for i in args.shapes.split(",")]
     peak, _ = _peaks()

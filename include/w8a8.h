@@ -69,8 +69,10 @@ enum {
     /* Every w8a8_gemm decode launch (M <= 32, and the row chunks of larger M) and every q8_0_gemv
      * launch is a programmatic dependent of the work queued before it on the stream, flag or not:
      * its CTAs may become resident and set themselves up while the previous kernel finishes, and
-     * touch no global memory until that kernel has completed and its writes are visible.  This
-     * needs nothing from the caller and behaves as plain stream order.
+     * read or write no global memory until that kernel has completed and its writes are visible.
+     * Before that point they only prefetch their first weight bytes into L2, a hint that changes
+     * no value any read returns.  This needs nothing from the caller and behaves as plain stream
+     * order.
      * W8A8_FLAG_PDL (programmatic dependent launch with weight prefetch) also lets the kernel start
      * streaming the packed weight (W_packed, or q, d and gamma of q8_0_gemv) before that point;
      * every other input, the output and the workspace are still touched only after it.  The caller
@@ -170,8 +172,8 @@ int w8a8_pack_weights(const int8_t* W, int K, int N, void* W_packed, void* ws, s
  *           blocks < T the tiles are laid end to end and CTA i takes a contiguous run of
  *           ceil or floor(T KB / (u blocks)) units of u slabs (the longer runs first), u being
  *           the plan's split_unit (1 or 4; see w8a8_plan_t).  0 = automatic: twice the SM
- *           count, at most one CTA per slab; for M <= 16 with that count >= T, rounded down to a
- *           multiple of T so that every tile is cut into the same number of parts.  Must not
+ *           count, at most one CTA per slab; for K <= 4096 with that count >= T, rounded down
+ *           to a multiple of T so that every tile is cut into the same number of parts.  Must not
  *           exceed the number of slabs.
  *           For M > 32 the same rule applies to T = ceil(N/128) tiles of 128 rows (two packed
  *           tiles each) x KB units of 32 k, with one CTA per SM by default.

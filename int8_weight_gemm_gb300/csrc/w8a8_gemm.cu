@@ -291,10 +291,11 @@ __global__ void __launch_bounds__(kMulti ? kThreads : kThreadsNoCombine, 2)
 
   // Every launch is a programmatic dependent of the work before it on the stream (gemm_launch), so
   // a CTA may start while the previous kernel finishes.  Until the dependency wait (griddepcontrol
-  // .wait, after which that kernel's writes are visible) a CTA only sets itself up: parameters,
-  // barriers, shared memory.  With W8A8_FLAG_PDL (p.pdl) the producer also issues the first stages'
-  // weight copies before the CTA-wide barrier, the caller having promised that nothing in flight
-  // writes the weights; the activation boxes always wait.  Every copy of a stage lands on the
+  // .wait, after which that kernel's writes are visible) a CTA only sets itself up (parameters,
+  // barriers, shared memory) and prefetches its first stages' weight bytes into L2.  With
+  // W8A8_FLAG_PDL (p.pdl) the producer instead issues those stages' weight copies into shared
+  // memory before the CTA-wide barrier, the caller having promised that nothing in flight writes
+  // the weights; the activation boxes always wait.  Every copy of a stage lands on the
   // stage's full barrier, which counts the weight and activation bytes together.
   const uint32_t xbox = (uint32_t)L::kXRawStage;
   StageIter it(b0, b1, p.KB, kStageSlabs, kMulti);   // producer: the next stage to issue
@@ -747,14 +748,16 @@ int gemm_plan(int M, int K, int N, int blocks, int sm_count, GemmPlan* plan) {
     // little in the split-tile combine, which costs one round trip.
     const long long g = (long long)kAutoCtasPerSm * (sm_count > 0 ? sm_count : 152);
     long long gg = g < pl.slabs ? g : pl.slabs;
-    // At M <= 16, with a CTA or more per tile, every tile is cut into the same number of parts
-    // (the largest multiple of the tile count that fits): the longest part is no longer, so no
-    // CTA streams more than with the extra CTAs, and the HBM share of each CTA grows.  Measured
-    // on GB300 (M = 16, graph replays): K = 12288, N = 4096 12.24 -> 11.54 us (256 CTAs), K = 4096,
-    // N = 8192 9.51 -> 9.08 (256), N = 12288 12.60 -> 12.20 (192), N = 1536 4.69 -> 4.65 (288);
-    // 11 of 12 shapes faster.  At M = 32 the consumer warps, not the stream, set the pace, and the
-    // extra CTAs win (K = 12288, N = 4096: 18.52 against 19.10 us), so larger M keeps them.
-    if (pl.nt8 <= 2 && gg >= pl.n_tiles) gg = (long long)pl.n_tiles * (gg / pl.n_tiles);
+    // With K <= 4096 and a CTA or more per tile, every tile is cut into the same number of parts
+    // (the largest multiple of the tile count that fits): the longest part is no longer, no CTA
+    // streams more than with the extra CTAs, and the HBM share of each CTA grows.  Measured on
+    // GB300 (graph replays, weights L2-prefetched before the dependency wait): M = 16, K = 4096,
+    // N = 12288 12.87 -> 11.89 us (192 CTAs), N = 8192 8.34 -> 8.16 (256), N = 2560 5.01 -> 4.92
+    // (280), K = 2048, N = 4096 4.67 -> 4.51 (256); M = 32, N = 2560 6.96 -> 6.78.  With longer
+    // tiles the extra CTAs win, their prefetch covering more of the stream before the wait
+    // (K = 12288, N = 4096: 10.52 us at 304 CTAs against 10.75 at 256; K = 14336 11.65 against
+    // 12.08), so K > 4096 keeps them.
+    if (pl.kb <= 128 && gg >= pl.n_tiles) gg = (long long)pl.n_tiles * (gg / pl.n_tiles);
     pl.blocks = (int)gg;
   } else {
     if (blocks > pl.slabs) return W8A8_ERR_INVALID_ARG;
@@ -800,9 +803,10 @@ static cudaError_t launch_gemm(const GemmParams& p, int blocks, int threads, cud
   cfg.blockDim = dim3((unsigned)threads);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
-  // Always a programmatic dependent of the work before it: the kernel touches no global memory
-  // before its dependency wait unless W8A8_FLAG_PDL allows the weight stream to start (p.pdl), so
-  // the overlap with the previous kernel's tail needs nothing from the caller.  Measured on GB300
+  // Always a programmatic dependent of the work before it: before its dependency wait the kernel
+  // reads or writes no global memory, only prefetches weight bytes into L2, unless W8A8_FLAG_PDL
+  // allows the weight stream to start (p.pdl), so the overlap with the previous kernel's tail
+  // needs nothing from the caller.  Measured on GB300
   // against plain launches (graph replays): gate_up M = 16 20.24 -> 19.42 us, M = 32 37.1 -> 33.6
   // us, the QKV-like shape 5.58 -> 4.65 us.
   cudaLaunchAttribute attr[1];

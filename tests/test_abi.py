@@ -136,8 +136,8 @@ def test_plan_shape_and_limits():
     p = lib8.w8a8_plan(16, 4096, 1536)
     assert p["n8_tiles"] == 2 and p["n_tiles"] == 24 and p["k_blocks"] == 128
     assert p["blocks"] == 288                                   # 12 parts of each of the 24 tiles (<= 2 CTAs per SM)
-    assert lib8.w8a8_plan(16, 12288, 4096)["blocks"] == 256      # 4 parts of each of the 64 tiles
-    assert lib8.w8a8_plan(32, 12288, 4096)["blocks"] == 304      # M > 16: two CTAs per SM (152 SMs without a GPU)
+    assert lib8.w8a8_plan(32, 2048, 4096)["blocks"] == 256       # 4 parts of each of the 64 tiles
+    assert lib8.w8a8_plan(16, 12288, 4096)["blocks"] == 304      # K > 4096: two CTAs per SM (152 SMs without a GPU)
     assert lib8.w8a8_plan(16, 4096, 24576)["blocks"] == 304      # fewer CTAs than tiles: two per SM
     assert lib8.w8a8_plan(1, 512, 256)["blocks"] == 64           # never more CTAs than slabs
     # a combine warp only when some CTA finishes more than one tile segment (fewer CTAs than tiles)
