@@ -118,6 +118,26 @@ def test_automatic_split_keeps_every_cta_inside_one_tile_for_small_outputs():
     assert all(b0 // 128 == (b1 - 1) // 128 for b0, b1 in zip(b[:-1], b[1:]))
 
 
+@pytest.mark.parametrize("M", [1, 8, 16, 24, 32])
+@pytest.mark.parametrize("K,N", [(4096, 1536), (4096, 2560), (2048, 4096), (4096, 6144), (4096, 8192),
+                                 (4096, 12288), (1024, 4096), (12288, 4096), (14336, 4096), (8192, 1536),
+                                 (4096, 24576), (512, 256)])
+def test_automatic_count_cuts_every_tile_equally_up_to_k_4096(M, K, N):
+    # The automatic CTA count: two per SM (152 SMs without a GPU), at most one per slab; with
+    # K <= 4096 and at least one CTA per tile, the largest multiple of the tile count that fits,
+    # so every tile is cut into the same number of parts, each within one slab of KB / c.
+    p = lib8.w8a8_plan(M, K, N)
+    T, KB, G = p["n_tiles"], p["k_blocks"], p["blocks"]
+    g = min(2 * 152, T * KB)
+    if KB <= 128 and g >= T:
+        assert G == T * (g // T)
+        c = G // T
+        sizes = np.diff(np.array(lib8.w8a8_split_bounds(K, N, G, M=M)))
+        assert sizes.max() - sizes.min() <= 1 and sizes.max() == -(-KB // c)
+    else:
+        assert G == g
+
+
 def test_split_slices_reproduce_the_oracle_sums():
     # Host replay of the plan: summing each CTA's k-slices of every tile in int32, in ascending CTA
     # order, must give the oracle's sums (the invariant behind the combine).
