@@ -322,7 +322,12 @@ int q8_0_gemv_rms(const void* x, const void* gamma, float eps, const int8_t* q, 
 /* x [M,K] bf16 row-major (16-byte aligned) -> x_q [M,K] int8 (8-byte aligned) and
  * x_scale [M] fp32: x_scale[m] = max_k |x[m][k]| / 127, x_q[m][k] = roundf(x[m][k] / x_scale[m]).
  * 1 <= M <= 2^20, 8 <= K <= 65536, K % 8 == 0.  Errors: INVALID_ARG, UNSUPPORTED_SHAPE,
- * MISALIGNED, CUDA. */
+ * MISALIGNED, CUDA.
+ * The kernel lets a programmatic dependent launched after it on the stream start at once
+ * (griddepcontrol.launch_dependents), so that a following w8a8_gemm prefetches its weights while
+ * it runs.  A dependent kernel of the caller's own must wait for the grid
+ * (griddepcontrol.wait or cudaGridDependencySynchronize) before it reads x_q or x_scale, as
+ * every kernel of this library does. */
 int w8a8_quantize_activations(const void* x, int8_t* x_q, float* x_scale, int M, int K, void* stream);
 
 /* Q8_0 from BF16 weights: w [N,K] bf16 row-major (16-byte aligned) -> the split layout of

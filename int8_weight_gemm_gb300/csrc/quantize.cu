@@ -56,6 +56,10 @@ __device__ __forceinline__ uint2 quantize8(const float (&f)[8], float s) {
 __global__ void __launch_bounds__(kRowThreads) quantize_rows_kernel(const uint4* __restrict__ x, uint2* __restrict__ xq,
                                                                     float* __restrict__ xs, int K) {
   __shared__ float red[kRowThreads / 32];
+  // A programmatic dependent launched after this grid (every decode GEMM launch is one) may start
+  // now: it prefetches its weights into L2 meanwhile, and waits for this grid to complete before
+  // it reads x_q or x_scale.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int row = blockIdx.x;
   const int nv = K / 8;
   const uint4* src = x + (size_t)row * nv;
